@@ -1,0 +1,106 @@
+"""Seeded synthetic inputs for the attention forward.
+
+This module holds only the input recipe (shapes, value distributions, seed):
+no attention arithmetic.  Both the GPU tests/benchmark and the CPU oracle
+consume what it generates; neither side's arithmetic lives here.
+
+The shapes are the workloads the pages benchmark or that this library is
+specified on.  The one shape the pages print is the RTX 5090 benchmark of
+"Hacker News Digest — gpu-computing", section "Flash Attention на 5090 в CUDA
+C++" (bs=1, heads=8, q=4096, kv=8192, BF16; head_dim 128 from the note that
+head_dim=128 fits in registers).  The other four are the tiny parity case,
+a causal D=64 batch, causal grouped-query attention and a long causal
+sequence with large logits.
+
+Recipe (all configs): one CPU ``torch.Generator`` seeded with ``seed``
+draws Q, then K, then V as float32 ``randn`` (Q multiplied by ``q_std`` in
+float32 first), each rounded to bf16 (round-to-nearest-even).  For the
+large-logit config, after V, each (batch, kv head) draws
+``randperm(Nkv)[:round(0.01 * Nkv)]`` and multiplies those K rows by 8 in
+float32 before the bf16 rounding (exact either way).  The scale is the
+float32 value of 1/sqrt(D).
+"""
+
+import math
+from dataclasses import dataclass, asdict
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Nq: int
+    Nkv: int
+    D: int
+    causal: bool
+    q_std: float = 1.0
+    k_spike_frac: float = 0.0
+    k_spike_mult: float = 1.0
+
+    @property
+    def scale(self):
+        """float32 value of 1/sqrt(D), as a Python float."""
+        return float(torch.tensor(1.0 / math.sqrt(self.D), dtype=torch.float32))
+
+    @property
+    def flops(self):
+        """Algorithmic flops of the forward: 4*B*Hq*Nq*Nkv*D, halved if
+        causal (the metric's convention)."""
+        f = 4.0 * self.B * self.Hq * self.Nq * self.Nkv * self.D
+        return f / 2 if self.causal else f
+
+    def as_dict(self):
+        return asdict(self)
+
+
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("tiny_128_d64", 1, 1, 1, 128, 128, 64, False),
+        Workload("pages_b1_h8_q4096_kv8192_d128", 1, 8, 8, 4096, 8192, 128,
+                 False),
+        Workload("causal_b4_h16_n2048_d64", 4, 16, 16, 2048, 2048, 64, True),
+        Workload("causal_gqa_b2_hq32_hkv8_n8192_d128", 2, 32, 8, 8192, 8192,
+                 128, True),
+        Workload("causal_b1_h16_n32768_d128_large_logits", 1, 16, 16, 32768,
+                 32768, 128, True, q_std=3.0, k_spike_frac=0.01,
+                 k_spike_mult=8.0),
+    ]
+}
+
+# The configuration the throughput metric is quoted on (the pages' shape).
+HEADLINE = "pages_b1_h8_q4096_kv8192_d128"
+
+
+def make_inputs(w, seed=0, device="cpu"):
+    """Generate (q, k, v) bf16 tensors [B,H,N,D] for workload ``w``.
+
+    Always drawn on the CPU generator (so every consumer sees identical
+    values), then moved to ``device``.
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    q = torch.randn(w.B, w.Hq, w.Nq, w.D, generator=g, dtype=torch.float32)
+    if w.q_std != 1.0:
+        q.mul_(w.q_std)
+    k = torch.randn(w.B, w.Hkv, w.Nkv, w.D, generator=g, dtype=torch.float32)
+    v = torch.randn(w.B, w.Hkv, w.Nkv, w.D, generator=g, dtype=torch.float32)
+    if w.k_spike_frac > 0:
+        n = int(round(w.k_spike_frac * w.Nkv))
+        for b in range(w.B):
+            for h in range(w.Hkv):
+                rows = torch.randperm(w.Nkv, generator=g)[:n]
+                k[b, h, rows] *= w.k_spike_mult
+    out = tuple(t.to(torch.bfloat16) for t in (q, k, v))
+    if device != "cpu":
+        out = tuple(t.to(device) for t in out)
+    return out
+
+
+def make_custom(B, Hq, Hkv, Nq, Nkv, D, seed=0, q_std=1.0):
+    """Seeded N(0,1) bf16 inputs of an arbitrary shape (edge-case tests)."""
+    w = Workload("custom", B, Hq, Hkv, Nq, Nkv, D, False, q_std=q_std)
+    return make_inputs(w, seed)
