@@ -1,0 +1,368 @@
+"""Benchmark of the attention forward on GB300: prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one attention forward (every step of the method: tiling, online
+softmax, both contractions, epilogue) over the workload's whole batch.  The
+default workload is the pages' benchmark shape (B=1, H=8, Nq=4096, Nkv=8192,
+D=128, non-causal, bf16).  The metric is TFLOPS = 4*B*Hq*Nq*Nkv*D (halved
+when causal) / time.
+
+Timing: inputs resident in HBM; L2 is flushed (a 512 MiB write) before every
+timed step, outside the step's CUDA-event pair, since the inputs are smaller
+than L2; events are recorded on the stream the kernel is launched on; the
+timed loop is bracketed by a barrier and a device synchronisation; the slowest
+rank's time counts.  With N>1 (torchrun) every rank runs its own replica of
+the workload (the method partitions by batch and head, with no exchange), so
+``value`` is the work of all ranks over the slowest rank's time (weak
+scaling).
+
+``--impl reference`` times the CPU oracle (float64, host cores) on bounded
+samples of the same workload: one 128-row query tile per step.
+"""
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_io_aware_fa2_gb300.workloads import (HEADLINE, WORKLOADS,  # noqa
+                                                make_inputs)
+
+METRIC = ("attention fwd TFLOPS (4·B·H·Nq·Nkv·D, "
+          "causal ½) and % of GB300 BF16 peak")
+UNIT = "TFLOPS"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "MEASURED_PEAKS.json bf16_tflops (burst)"
+    return FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(
+            ROOT, "exact_io_aware_fa2_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_src_sha") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(w, q, k, v, seconds):
+    """The oracle as it stands, on this host's cores, on whole heads of the
+    workload until about ``seconds`` of CPU work (at least one head)."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    torch.set_num_threads(cores)
+    group = w.Hq // w.Hkv
+    t0 = time.perf_counter()
+    heads = 0
+    for b in range(w.B):
+        for h in range(w.Hq):
+            hk = h // group
+            oracle.attention_fp64(q[b:b + 1, h:h + 1], k[b:b + 1, hk:hk + 1],
+                                  v[b:b + 1, hk:hk + 1], w.scale, w.causal)
+            heads += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    flops = w.flops / (w.B * w.Hq) * heads
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": f"{heads} of {w.B * w.Hq} (batch, head) slices of "
+                      f"{w.name}, float64, {dt:.1f} s"}
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    torch.set_num_threads(cores)
+    q, k, v = make_inputs(w)
+    group = w.Hq // w.Hkv
+    n_tiles = (w.Nq + 127) // 128
+    units = [(b, h, t) for b in range(w.B) for h in range(w.Hq)
+             for t in range(n_tiles)]
+
+    def step(i):
+        b, h, t = units[i % len(units)]
+        rows = list(range(t * 128, min(w.Nq, t * 128 + 128)))
+        oracle.attention_rows_fp64(q, k, v, w.scale, w.causal, b, h, rows)
+        kv = min(w.Nkv, rows[-1] + 1) if w.causal else w.Nkv
+        # flops of this tile, counted like the metric (causal: visible half)
+        vis = sum(min(r + 1, w.Nkv) for r in rows) if w.causal else \
+            len(rows) * kv
+        return 4.0 * vis * w.D
+
+    for i in range(args.warmup):
+        step(i)
+    flops = 0.0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flops += step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    val = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, **w.as_dict(),
+                   "sample": "one 128-row query tile per step"},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores,
+                         "kind": "oracle",
+                         "sample": "one 128-row query tile of the workload "
+                                   "per step, float64"},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    from exact_io_aware_fa2_gb300 import fa
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    q_h, k_h, v_h = make_inputs(w)
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.Nq, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def launch():
+        fa.fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse)
+
+    for _ in range(max(3, args.warmup)):
+        launch()
+    torch.cuda.synchronize(dev)
+    if fa.last_device_error() != 0:
+        raise RuntimeError("bounded-wait timeout during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    smi_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(dev.index))
+                    .split(",")[dev.index]) if os.environ.get(
+        "CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else dev.index
+    with ClockSampler(smi_index) as clk:
+        time.sleep(0.3)
+        barrier()
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))                    # evict L2 (untimed)
+            starts[i].record(stream)
+            launch()
+            ends[i].record(stream)
+        barrier()
+        wall = time.perf_counter() - wall0
+    if fa.last_device_error() != 0:
+        raise RuntimeError("bounded-wait timeout during the timed loop")
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(per) / len(per)
+    ms_max = ms
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = ws * w.flops / (ms_max * 1e-3) / 1e12
+    per_launch_tflops = w.flops / (ms * 1e-3) / 1e12
+    peak, peak_src = peaks()
+
+    # ---- end to end through the public API with host buffers ----
+    qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
+    bufs = fa.host_buffers(qp, kp, vp, device=dev)
+    for _ in range(3):
+        fa.fwd_host(qp, kp, vp, scale=w.scale, causal=w.causal, bufs=bufs)
+    e2e_steps = max(5, min(args.steps, 50))
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        fa.fwd_host(qp, kp, vp, scale=w.scale, causal=w.causal, bufs=bufs)
+    barrier()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if ws > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, q_h, k_h, v_h, args.cpu_seconds)
+
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+    dev_name = torch.cuda.get_device_name(dev)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "pct_of_peak": 100.0 * per_launch_tflops / peak,
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "Nq": w.Nq, "Nkv": w.Nkv, "D": w.D, "causal": w.causal,
+                   "scale": w.scale, "seed": 0, "global_batch": w.B * ws,
+                   "parallelism": f"replicas{ws}" if ws > 1 else "single",
+                   "l2": "flushed (512 MiB write) before every timed step",
+                   "device": dev_name},
+        "roofline": {"bound": "tensor", "achieved": per_launch_tflops,
+                     "peak": peak, "unit": "TFLOP/s",
+                     "frac": per_launch_tflops / peak,
+                     "peak_source": peak_src + ", of measured"
+                     if "MEASURED" in peak_src else peak_src + ", of fallback",
+                     "traffic": recorded_traffic(w.name),
+                     "kernel": "fa_fwd_kernel",
+                     "algorithmic_flops_per_launch": w.flops},
+        "cpu_baseline": cpu,
+        "e2e": {"value": w.flops * ws / e2e_s / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_loop": wall,
+        "ms_per_step_min": min(per), "ms_per_step_median":
+            statistics.median(per),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

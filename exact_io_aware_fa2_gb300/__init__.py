@@ -6,11 +6,12 @@ load the library; the first call into ``fa`` does, and raises if it is
 missing (there is no CPU fallback).
 """
 
+import importlib
+
 from . import workloads  # noqa: F401
 
 
 def __getattr__(name):
-    if name in ("fwd", "fa"):
-        from . import fa as _fa
-        return _fa if name == "fa" else _fa.fwd
+    if name == "fwd":
+        return importlib.import_module(".fa", __name__).fwd
     raise AttributeError(name)

@@ -1,0 +1,168 @@
+"""ctypes binding of the C ABI in ``include/fa.h`` (``libfa_gb300.so``).
+
+Argument marshalling only: tensors become device pointers and sizes, the
+current torch stream becomes the ``stream`` argument, and a nonzero status
+becomes an exception.  Every step of the computation runs in the library's
+kernels; there is no fallback of any kind — if the library is missing or the
+device is not sm_103, calls raise.
+
+    o, lse = fwd(q, k, v, scale=None, causal=False)
+
+q: bf16 [B, Hq, Nq, D]; k, v: bf16 [B, Hkv, Nkv, D]; all CUDA, contiguous.
+Returns o (bf16, like q) and lse (fp32 [B, Hq, Nq]).  ``fwd_host`` does the
+same for pinned host tensors: it copies the inputs to the device, runs the
+kernel and copies O and LSE back, all on the current stream.
+"""
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from .build import LIB_PATH
+
+FA_OK = 0
+STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_VALUE", 2: "FA_ERR_UNSUPPORTED",
+                3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
+# Every symbol the header declares.
+SYMBOLS = ("fa_fwd", "fa_status_string", "fa_last_device_error",
+           "fa_probe_bounded_wait", "fa_version")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class FAError(RuntimeError):
+    def __init__(self, status, what="fa_fwd"):
+        self.status = status
+        super().__init__(f"{what} failed: {STATUS_NAMES.get(status, status)}")
+
+
+def library_path():
+    return LIB_PATH
+
+
+def load():
+    """Load (once) and return the ctypes handle of the library."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{os.path.basename(LIB_PATH)} is not built; run "
+                "`python -c \"import __graft_entry__ as g; g.build()\"`")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, ci = ctypes.c_void_p, ctypes.c_int
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci,
+                               ctypes.c_float, ci, vp]
+        lib.fa_fwd.restype = ci
+        lib.fa_status_string.argtypes = [ci]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_last_device_error.argtypes = []
+        lib.fa_last_device_error.restype = ci
+        lib.fa_probe_bounded_wait.argtypes = [ctypes.c_longlong, vp]
+        lib.fa_probe_bounded_wait.restype = ci
+        lib.fa_version.argtypes = []
+        lib.fa_version.restype = ci
+        _lib = lib
+        return lib
+
+
+def status_string(status):
+    return load().fa_status_string(int(status)).decode()
+
+
+def last_device_error():
+    return int(load().fa_last_device_error())
+
+
+def probe_bounded_wait(timeout_ns, stream=None):
+    st = stream if stream is not None else torch.cuda.current_stream()
+    return int(load().fa_probe_bounded_wait(int(timeout_ns),
+                                            ctypes.c_void_p(st.cuda_stream)))
+
+
+def _check(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [B, H, N, D]")
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    B, Hq, Nq, D = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError("k, v must be [B, Hkv, Nkv, D] matching q")
+    return B, Hq, k.shape[1], Nq, k.shape[2], D
+
+
+def fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, Nq, Nkv, D,
+            scale, causal, stream_handle):
+    """Direct call of ``fa_fwd`` with integer pointers; returns the status."""
+    return int(load().fa_fwd(
+        ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+        ctypes.c_void_p(o_ptr), ctypes.c_void_p(lse_ptr),
+        B, Hq, Hkv, Nq, Nkv, D, ctypes.c_float(scale), 1 if causal else 0,
+        ctypes.c_void_p(stream_handle)))
+
+
+def fwd(q, k, v, scale=None, causal=False, out=None, lse=None,
+        want_lse=True):
+    """Attention forward through the C ABI on the current CUDA stream."""
+    B, Hq, Hkv, Nq, Nkv, D = _check(q, k, v)
+    dev = q.device
+    if dev.type != "cuda" or k.device != dev or v.device != dev:
+        raise ValueError("q, k, v must be CUDA tensors on one device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if want_lse and lse is None:
+        lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                     lse.data_ptr() if lse is not None else 0,
+                     B, Hq, Hkv, Nq, Nkv, D, scale, causal, stream)
+    if st != FA_OK:
+        raise FAError(st)
+    return out, lse
+
+
+def fwd_host(q, k, v, scale=None, causal=False, device="cuda", bufs=None):
+    """Forward on host tensors: copy in (pinned -> device), run, copy out.
+
+    ``bufs`` may hold preallocated device buffers (q, k, v, o, lse) and
+    pinned host outputs (o_h, lse_h) to reuse across calls.  Returns host
+    (o, lse); the copies and the kernel are ordered on the current stream,
+    and the call synchronises that stream before returning.
+    """
+    _check(q, k, v)
+    if bufs is None:
+        bufs = host_buffers(q, k, v, device)
+    bufs["q"].copy_(q, non_blocking=True)
+    bufs["k"].copy_(k, non_blocking=True)
+    bufs["v"].copy_(v, non_blocking=True)
+    fwd(bufs["q"], bufs["k"], bufs["v"], scale=scale, causal=causal,
+        out=bufs["o"], lse=bufs["lse"])
+    bufs["o_h"].copy_(bufs["o"], non_blocking=True)
+    bufs["lse_h"].copy_(bufs["lse"], non_blocking=True)
+    torch.cuda.current_stream(bufs["o"].device).synchronize()
+    return bufs["o_h"], bufs["lse_h"]
+
+
+def host_buffers(q, k, v, device="cuda"):
+    """Device inputs/outputs and pinned host outputs for ``fwd_host``."""
+    B, Hq, Nq, D = q.shape
+    return {
+        "q": torch.empty(q.shape, dtype=q.dtype, device=device),
+        "k": torch.empty(k.shape, dtype=k.dtype, device=device),
+        "v": torch.empty(v.shape, dtype=v.dtype, device=device),
+        "o": torch.empty(q.shape, dtype=q.dtype, device=device),
+        "lse": torch.empty(B, Hq, Nq, dtype=torch.float32, device=device),
+        "o_h": torch.empty(q.shape, dtype=q.dtype).pin_memory(),
+        "lse_h": torch.empty(B, Hq, Nq, dtype=torch.float32).pin_memory(),
+    }

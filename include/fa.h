@@ -1,0 +1,109 @@
+/*
+ * fa.h — C ABI of the exact, IO-aware attention forward for GB300 (sm_103a).
+ *
+ * Operation (per batch b, query head h, query row i):
+ *     S_ij   = scale * <Q[b,h,i,:], K[b,g,j,:]>,   g = h / (Hq / Hkv)
+ *     O[b,h,i,:] = sum_j softmax_j(S_i.) * V[b,g,j,:]      over visible j
+ *     LSE[b,h,i] = ln sum_j exp(S_ij)                       over visible j
+ * with "visible" = every key when causal == 0, and key j <= query i when
+ * causal != 0 (top-left alignment, for any Nq, Nkv).
+ *
+ * Where it is defined:
+ *   - "flash attention v3 paper" search page (cidian.kuaisou.com), first
+ *     snippet: standard attention S = QK^T, P = row-softmax(S), O = PV
+ *     (scale and mask omitted there);
+ *   - "Hacker News Digest — gpu-computing" (hckr.top), section "Алгоритм
+ *     Flash Attention 2": scale = DIM**-0.5 multiplies Q K^T, the loop over
+ *     (batch, query tile) and over key/value tiles with an in-place online
+ *     softmax; section "v1 — базовая версия", item 3: the running max and
+ *     denominator recurrence;
+ *   - "Flash Attention (Kutarisa Kwemheni)" (aiunderstanding.org), summary
+ *     and FAQ: the result is exact attention, computed tile by tile so the
+ *     N x N score matrix never reaches HBM.
+ * GQA head sharing and the LSE output are this library's specification; the
+ * pages do not define them.
+ *
+ * All functions are thread-safe and callable from any host thread.  The
+ * library allocates no device memory.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_VALUE = 1, /* null pointer, dimension < 1, Hq % Hkv != 0,
+                                 non-finite scale, size beyond the limits   */
+    FA_ERR_UNSUPPORTED = 2,   /* D not in {64, 128}, or the current device is
+                                 not compute capability 10.3 (sm_103)       */
+    FA_ERR_MISALIGNED = 3,    /* q, k, v or o not 16-byte aligned, or lse not
+                                 4-byte aligned (TMA needs 16 bytes)        */
+    FA_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (launch,
+                                 device query, tensor-map encoding)         */
+    FA_ERR_TIMEOUT = 5        /* a kernel's bounded wait ran out (reported by
+                                 fa_last_device_error after a sync)         */
+} fa_status;
+
+/*
+ * fa_fwd — attention forward on bf16 tensors, fp32 log-sum-exp.
+ *
+ *   q    device pointer, bf16 [B, Hq,  Nq,  D], contiguous (row-major)
+ *   k    device pointer, bf16 [B, Hkv, Nkv, D], contiguous
+ *   v    device pointer, bf16 [B, Hkv, Nkv, D], contiguous
+ *   o    device pointer, bf16 [B, Hq,  Nq,  D], contiguous; written
+ *   lse  device pointer, fp32 [B, Hq,  Nq], contiguous; written; may be NULL
+ *   B, Hq, Hkv, Nq, Nkv, D   sizes; Hq must be a multiple of Hkv (query head
+ *        h reads kv head h / (Hq / Hkv)); D in {64, 128}
+ *   scale  finite fp32 multiplier of Q K^T (typically 1/sqrt(D))
+ *   causal 0: every key visible; nonzero: key j visible to query i iff j <= i
+ *   stream a cudaStream_t (as void*); NULL means the legacy default stream
+ *
+ * Ownership: the caller owns every buffer; nothing is retained after the
+ * call returns.  o and lse must not overlap q, k, v or each other.
+ *
+ * Behaviour: arguments are validated on the host and an error is returned
+ * before anything is launched; on FA_OK the work is enqueued on `stream`
+ * and the call returns without synchronising.  Faults during execution
+ * surface at the next synchronisation of that stream; a bounded wait that
+ * ran out is reported by fa_last_device_error().  O is rounded to bf16
+ * (round-to-nearest-even); arithmetic is fp32 with bf16 tensor-core inputs.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+           float scale, int causal, void* stream);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* fa_status_string(int status);
+
+/*
+ * fa_last_device_error — FA_OK, or FA_ERR_TIMEOUT if any kernel of this
+ * library on the current device gave up a bounded wait since the previous
+ * query.  Reads and clears a device-side word (synchronising copy); call it
+ * after synchronising the streams the kernels ran on.  Returns FA_ERR_CUDA
+ * if the word cannot be read.
+ */
+int fa_last_device_error(void);
+
+/*
+ * fa_probe_bounded_wait — enqueue a one-warp kernel on `stream` that waits
+ * on a shared-memory barrier nothing will ever complete, with a limit of
+ * `timeout_ns` nanoseconds (1 .. 10^9), then records FA_ERR_TIMEOUT in the
+ * device word read by fa_last_device_error() and returns.  It exercises the
+ * same bounded-wait routine the attention kernel uses, so a caller can check
+ * that an expired wait ends in an error status instead of a hang.
+ * Returns FA_ERR_INVALID_VALUE for a limit outside the range.
+ */
+int fa_probe_bounded_wait(long long timeout_ns, void* stream);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

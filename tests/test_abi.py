@@ -1,0 +1,107 @@
+"""The C-ABI library: builds, loads, exports every declared symbol, and
+rejects bad arguments on the host before touching the GPU (CPU only)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_io_aware_fa2_gb300 import build as fabuild
+from exact_io_aware_fa2_gb300 import fa
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include",
+                      "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(fabuild.LIB_PATH):
+        fabuild.build()
+    return fa.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(fa_\w+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_header_declares_the_expected_entry_points():
+    assert _declared_functions() == sorted(fa.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    # and they are real exported C symbols (not C++-mangled)
+    raw = ctypes.CDLL(fabuild.LIB_PATH)
+    for name in _declared_functions():
+        getattr(raw, name)
+
+
+def test_status_strings(lib):
+    for code, name in fa.STATUS_NAMES.items():
+        assert fa.status_string(code) == name
+    assert fa.status_string(99) == "FA_ERR_UNKNOWN"
+    assert lib.fa_version() == 100
+
+
+P = 1 << 20  # a 16-byte-aligned stand-in address; never dereferenced
+
+
+def _call(**kw):
+    args = dict(q=P, k=P, v=P, o=P, lse=P, B=1, Hq=2, Hkv=1, Nq=128, Nkv=128,
+                D=64, scale=0.125, causal=0, stream=0)
+    args.update(kw)
+    return fa.fwd_raw(args["q"], args["k"], args["v"], args["o"], args["lse"],
+                      args["B"], args["Hq"], args["Hkv"], args["Nq"],
+                      args["Nkv"], args["D"], args["scale"], args["causal"],
+                      args["stream"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=0), dict(k=0), dict(v=0), dict(o=0),
+    dict(B=0), dict(Hq=0), dict(Hkv=0), dict(Nq=0), dict(Nkv=0), dict(D=0),
+    dict(B=-1), dict(Nkv=-5),
+    dict(Hq=3, Hkv=2), dict(Hq=2, Hkv=4),
+    dict(scale=float("nan")), dict(scale=float("inf")),
+    dict(B=70000), dict(Hq=70000, Hkv=1),
+])
+def test_invalid_values_rejected_before_launch(lib, kw):
+    assert _call(**kw) == 1  # FA_ERR_INVALID_VALUE
+
+
+@pytest.mark.parametrize("D", [1, 16, 32, 80, 96, 192, 256])
+def test_unsupported_head_dims(lib, D):
+    assert _call(D=D) == 2  # FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw", [dict(q=P + 2), dict(k=P + 8), dict(v=P + 4),
+                                dict(o=P + 1), dict(lse=P + 2)])
+def test_misaligned_pointers_rejected(lib, kw):
+    assert _call(**kw) == 3  # FA_ERR_MISALIGNED
+
+
+def test_lse_may_be_null_for_validation(lib):
+    # a null lse is legal; with everything else invalid the error is still
+    # the validation one
+    assert _call(lse=0, q=0) == 1
+
+
+def test_probe_rejects_bad_limits(lib):
+    assert lib.fa_probe_bounded_wait(0, None) == 1
+    assert lib.fa_probe_bounded_wait(2_000_000_000, None) == 1
+
+
+def test_binding_rejects_bad_tensors():
+    import torch
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        fa._check(q, q, q)
+    qb = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa._check(qb, qb[:, :, :4], qb)
+    with pytest.raises(ValueError):
+        fa._check(qb.transpose(2, 3), qb, qb)
