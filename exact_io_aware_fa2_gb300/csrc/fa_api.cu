@@ -126,7 +126,8 @@ template <int D, bool CAUSAL>
 int launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
            const fa::FwdParams& p, int B, int Hq, int Nq,
            cudaStream_t stream) {
-  dim3 grid((Nq + fa::kBM - 1) / fa::kBM, Hq, B);
+  const int rows_per_cta = fa::kBM * fa::kTilesPerCta;
+  dim3 grid((Nq + rows_per_cta - 1) / rows_per_cta, Hq, B);
   fa::fa_fwd_kernel<D, CAUSAL>
       <<<grid, fa::kThreads, fa::FwdCfg<D>::kSmemBytes, stream>>>(q, k, v, p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;

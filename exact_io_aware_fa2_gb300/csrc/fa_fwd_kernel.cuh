@@ -5,28 +5,41 @@
 // S = Q K^T * scale, apply the online softmax in place, accumulate S @ V),
 // with the running max / denominator of section "v1 — базовая версия",
 // item 3, and the FA2 work split of the "flash attention v3 paper" search
-// page, third snippet (one thread block owns one row block of O and walks
-// all key/value blocks).  The division by the denominator is deferred to
-// the epilogue (the same result as renormalising each tile, which the
-// pages print).
+// page, third snippet (a thread block owns row blocks of O and walks all
+// key/value blocks for them).  The division by the denominator is deferred
+// to the epilogue, which gives the same result as the per-tile
+// renormalisation the pages print.
 //
-// One CTA owns one 128-row query tile of one (batch, query head).  Warp
-// roles (192 threads):
-//   warps 0-3  softmax: thread t owns query row t (TMEM lane t); reads S from
-//              TMEM, masks, tracks the running max m and sum l (log2 domain,
-//              scale folded into one FFMA), writes P = exp2(...) as bf16 into
-//              TMEM, rescales the O accumulator in TMEM when m grows, and
-//              finally writes O / l and LSE.
-//   warp 4     TMA producer: Q once, then K_j and V_j into two rings of
-//              NSTAGE shared-memory stages (128-byte swizzle).
-//   warp 5     MMA issuer (one thread): S_j = Q K_j^T (both operands in
-//              shared memory, K-major) and O += P_j V_j (P from TMEM, V from
-//              shared memory, MN-major), accumulators in TMEM.
+// One CTA owns two 128-row query tiles (A: rows r0..r0+127, B: the next 128
+// rows) of one (batch, query head); both share every K/V block the CTA
+// loads.  Warp roles (320 threads):
+//   warps 0-3  softmax of tile A: thread t owns query row r0+t (TMEM lane t)
+//   warps 4-7  softmax of tile B (same lanes, its own TMEM columns)
+//              each reads S from TMEM, masks the causal diagonal / ragged
+//              tail, keeps the row's reference max m and sum l in the log2
+//              domain (scale folded into one FFMA), writes P = exp2(s*c - m)
+//              as bf16 into TMEM, rescales its O accumulator in TMEM when m
+//              moves, and finally writes O / l and the LSE.
+//   warp 8     TMA producer: Q_A and Q_B once, then K_j and V_j into two
+//              rings of shared-memory stages (128-byte swizzle).
+//   warp 9     MMA issuer (one thread), in the order
+//                 PV_A(j-1), S_A(j), PV_B(j-1), S_B(j), PV_A(j), ...
+//              so the tensor pipe works on one tile while the other tile's
+//              softmax runs.  S = Q K^T has both operands in shared memory
+//              (K-major); O += P V takes P from TMEM and V (MN-major) from
+//              shared memory.
 //
-// TMEM columns (512 allocated): S double buffer at 0 and 128, O at 256
-// (D columns), P double buffer at 384 and 448 (64 columns of packed bf16x2
-// each).  Nothing larger than one 128x128 score tile ever exists, and only
-// on chip.
+// The reference max m is moved lazily: only when a block's max exceeds it
+// by more than kRescaleLog2 (a factor 2^8).  O, l and every later p use the
+// same m, so the result is exact either way; the threshold only bounds the
+// size of p (<= 2^8) and of l and O (far below fp32 overflow).
+//
+// TMEM columns (512 allocated): S_A at 0, S_B at 128, O_A at 256, O_B after
+// it (D columns each).  At D=128 P overwrites the first 64 columns of its own
+// S (packed bf16x2) once the softmax has read S; the next S MMA into that
+// region is issued after the P*V MMA that reads it, and tcgen05 MMAs issued
+// by one thread execute in order.  At D=64 P has its own columns (384, 448).
+// Nothing larger than one 128x128 score tile exists, and only on chip.
 #pragma once
 
 #include "sm103_ptx.cuh"
@@ -34,24 +47,39 @@
 namespace fa {
 
 constexpr int kBM = 128;          // query rows per tile (TMEM lanes)
-constexpr int kBN = 128;          // keys per tile
+constexpr int kBN = 128;          // keys per K/V block
+constexpr int kTilesPerCta = 2;
 constexpr int kBoxCols = 64;      // bf16 elements per 128-byte swizzle row
 constexpr int kBoxBytes = kBM * kBoxCols * 2;   // one TMA box: 128 x 64 bf16
-constexpr int kThreads = 192;
-
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP0 = 384,
-                   kColP1 = 448, kTmemCols = 512;
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr uint32_t kTmemCols = 512;
 
 template <int D>
 struct FwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr int kTileBytes = kBM * D * 2;       // 16 KiB or 32 KiB
   static constexpr int kBoxes = D / kBoxCols;          // TMA boxes per tile
-  static constexpr int kStages = (D == 128) ? 3 : 4;   // K and V ring depth
-  static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 1 + 1 + 1;
+  static constexpr int kStages = (D == 128) ? 2 : 4;   // K and V ring depth
+  // barriers: Q, K full/empty, V full/empty, S full x2, P full x2, O final,
+  // drain
+  static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 1 + 1;
   static constexpr int kBarBytes = 8 * kNumBars + 16;  // + tmem slot + abort
   static constexpr int kSmemBytes =
-      1024 /*alignment slack*/ + kTileBytes * (1 + 2 * kStages) + kBarBytes;
+      1024 /*alignment slack*/ + kTileBytes * (kTilesPerCta + 2 * kStages) +
+      kBarBytes;
+  // TMEM column of tile x's S, O and P.
+  __host__ __device__ static constexpr uint32_t col_s(int x) {
+    return x ? 128u : 0u;
+  }
+  __host__ __device__ static constexpr uint32_t col_o(int x) {
+    return x ? 256u + D : 256u;
+  }
+  __host__ __device__ static constexpr uint32_t col_p(int x) {
+    return D == 128 ? col_s(x) : (x ? 448u : 384u);
+  }
   static constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);
 };
@@ -64,6 +92,13 @@ struct FwdParams {
   int* status;        // device status word (bounded-wait timeouts)
   uint64_t wait_limit_ns;
 };
+
+// Number of K/V blocks a tile starting at query row `row0` visits.
+template <bool CAUSAL>
+__device__ __forceinline__ int kv_blocks(int row0, int Nkv) {
+  const int end = CAUSAL ? min(Nkv, row0 + kBM) : Nkv;
+  return (end + kBN - 1) / kBN;
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -78,22 +113,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work item: (batch b, query head hq, query tile t) ----
-  const int n_qtiles = gridDim.x;
-  const int t = CAUSAL ? (n_qtiles - 1 - static_cast<int>(blockIdx.x))
-                       : static_cast<int>(blockIdx.x);
+  // ---- work item: (batch b, query head hq, tile pair) ----
+  const int n_pairs = gridDim.x;
+  const int pair = CAUSAL ? (n_pairs - 1 - static_cast<int>(blockIdx.x))
+                          : static_cast<int>(blockIdx.x);
   const int hq = blockIdx.y;
   const int b = blockIdx.z;
   const int hk = hq / (p.Hq / p.Hkv);
-  const int q_row0 = t * kBM;
-  const int kv_end = CAUSAL ? min(p.Nkv, q_row0 + kBM) : p.Nkv;
-  const int n_blocks = (kv_end + kBN - 1) / kBN;
+  const int row0[2] = {pair * (2 * kBM), pair * (2 * kBM) + kBM};
+  const bool has_b = row0[1] < p.Nq;
+  const int nblk[2] = {kv_blocks<CAUSAL>(row0[0], p.Nkv),
+                       has_b ? kv_blocks<CAUSAL>(row0[1], p.Nkv) : 0};
+  const int n_blocks = max(nblk[0], nblk[1]);
 
   // ---- shared memory carve-up (1024-byte aligned for the swizzle atoms) --
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - smem_addr(smem_raw));
-  const uint32_t sQ = base;
-  const uint32_t sK = sQ + C::kTileBytes;
+  const uint32_t sQ = base;                          // Q_A, then Q_B
+  const uint32_t sK = sQ + kTilesPerCta * C::kTileBytes;
   const uint32_t sV = sK + NS * C::kTileBytes;
   const uint32_t sBar = sV + NS * C::kTileBytes;
   auto bar = [&](int i) { return sBar + 8u * static_cast<uint32_t>(i); };
@@ -102,11 +139,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bKEmpty = [&](int s) { return bar(1 + NS + s); };
   auto bVFull = [&](int s) { return bar(1 + 2 * NS + s); };
   auto bVEmpty = [&](int s) { return bar(1 + 3 * NS + s); };
-  auto bSFull = [&](int i) { return bar(1 + 4 * NS + i); };
-  auto bSEmpty = [&](int i) { return bar(3 + 4 * NS + i); };
-  const uint32_t bPFull = bar(5 + 4 * NS);
-  const uint32_t bODone = bar(6 + 4 * NS);
-  const uint32_t bDrain = bar(7 + 4 * NS);
+  auto bSFull = [&](int x) { return bar(1 + 4 * NS + x); };
+  auto bPFull = [&](int x) { return bar(3 + 4 * NS + x); };
+  const uint32_t bOFinal = bar(5 + 4 * NS);
+  const uint32_t bDrain = bar(6 + 4 * NS);
   uint8_t* const misc = base_ptr + (sBar - base) + 8 * C::kNumBars;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile uint32_t* const abort = reinterpret_cast<uint32_t*>(misc + 4);
@@ -119,12 +155,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bVFull(s), 1);
       mbar_init(bVEmpty(s), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bSFull(i), 1);
-      mbar_init(bSEmpty(i), 4);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bSFull(x), 1);
+      mbar_init(bPFull(x), 4);
     }
-    mbar_init(bPFull, 4);
-    mbar_init(bODone, 1);
+    mbar_init(bOFinal, 1);
     mbar_init(bDrain, 1);
     *abort = 0u;
     mbar_init_fence();
@@ -139,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort, p.status, p.wait_limit_ns};
 
-  if (warp == 4) {
+  if (warp == kLoadWarp) {
     // ============================ TMA producer ============================
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -149,10 +184,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t once = l2_policy_evict_first();
       const int zq = b * p.Hq + hq;
       const int zk = b * p.Hkv + hk;
-      mbar_arrive_expect_tx(bQFull, C::kTileBytes);
-      for (int c = 0; c < C::kBoxes; ++c)
-        tma_load_3d(sQ + c * kBoxBytes, &tmQ, bQFull, c * kBoxCols, q_row0,
-                    zq, once);
+      mbar_arrive_expect_tx(bQFull, C::kTileBytes * (has_b ? 2 : 1));
+      for (int x = 0; x < (has_b ? 2 : 1); ++x)
+        for (int c = 0; c < C::kBoxes; ++c)
+          tma_load_3d(sQ + x * C::kTileBytes + c * kBoxBytes, &tmQ, bQFull,
+                      c * kBoxCols, row0[x], zq, once);
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_blocks; ++j) {
         const int s = j % NS;
@@ -178,85 +214,88 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(bVFull(j % NS), (j / NS) & 1, wc, false);
       mbar_wait(bQFull, 0, wc, false);
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ============================ MMA issuer ==============================
     if (lane == 0) {
       bool ok = mbar_wait(bQFull, 0, wc);
       for (int j = 0; ok && j <= n_blocks; ++j) {
-        if (j < n_blocks) {
-          const int s = j % NS;
-          const int sb = j & 1;
-          if (!(ok = mbar_wait(bKFull(s), (j / NS) & 1, wc))) break;
-          if (j >= 2 &&
-              !(ok = mbar_wait(bSEmpty(sb), ((j >> 1) - 1) & 1, wc)))
-            break;
-          tc_fence_after();
-          const uint32_t d_s = tmem + (sb ? kColS1 : kColS0);
-          const uint32_t k_base = sK + s * C::kTileBytes;
+        const int s = j % NS;
+        const int sp = (j + NS - 1) % NS;      // stage of block j-1
+        if (j < n_blocks && !(ok = mbar_wait(bKFull(s), (j / NS) & 1, wc)))
+          break;
+        if (j >= 1 &&
+            !(ok = mbar_wait(bVFull(sp), ((j - 1) / NS) & 1, wc)))
+          break;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            mma_ss(d_s, sdesc_sw128(sQ + off, 16, 1024),
-                   sdesc_sw128(k_base + off, 16, 1024), C::kIdescS,
-                   kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bSFull(sb));
-          mma_commit(bKEmpty(s));
-        }
-        if (j >= 1) {
-          const int jj = j - 1;
-          const int s = jj % NS;
-          if (!(ok = mbar_wait(bPFull, jj & 1, wc))) break;
-          if (!(ok = mbar_wait(bVFull(s), (jj / NS) & 1, wc))) break;
-          tc_fence_after();
-          const uint32_t a_p = tmem + ((jj & 1) ? kColP1 : kColP0);
-          const uint32_t v_base = sV + s * C::kTileBytes;
+        for (int x = 0; x < 2; ++x) {
+          // O_x += P_x(j-1) V_{j-1}
+          if (j >= 1 && j - 1 < nblk[x]) {
+            if (!(ok = mbar_wait(bPFull(x), (j - 1) & 1, wc))) break;
+            tc_fence_after();
+            const uint32_t a_p = tmem + C::col_p(x);
+            const uint32_t v_base = sV + sp * C::kTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            mma_ts(tmem + kColO, a_p + kk * 8,
-                   sdesc_sw128(v_base + kk * 2048, kBoxBytes, 1024),
-                   C::kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              mma_ts(tmem + C::col_o(x), a_p + kk * 8,
+                     sdesc_sw128(v_base + kk * 2048, kBoxBytes, 1024),
+                     C::kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(bODone);
-          mma_commit(bVEmpty(s));
+          // S_x(j) = Q_x K_j^T
+          if (j < nblk[x]) {
+            tc_fence_after();
+            const uint32_t q_base = sQ + x * C::kTileBytes;
+            const uint32_t k_base = sK + s * C::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+              mma_ss(tmem + C::col_s(x), sdesc_sw128(q_base + off, 16, 1024),
+                     sdesc_sw128(k_base + off, 16, 1024), C::kIdescS,
+                     kk > 0 ? 1u : 0u);
+            }
+            mma_commit(bSFull(x));
+          }
         }
+        if (!ok) break;
+        if (j < n_blocks) mma_commit(bKEmpty(s));
+        if (j >= 1) mma_commit(bVEmpty(sp));
       }
+      mma_commit(bOFinal);
       // Every MMA this thread issued completes before the CTA tears down.
       mma_commit(bDrain);
       mbar_wait(bDrain, 0, wc, false);
     }
   } else {
     // ============================ softmax warps ===========================
-    const int row = threadIdx.x;                 // 0..127 == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int x = warp >> 2;                       // tile A (0) or B (1)
+    const int nb = x ? nblk[1] : nblk[0];
+    const int my_row0 = x ? row0[1] : row0[0];
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float c = p.scale_log2;
     const bool neg_scale = c < 0.f;
-    const int q_abs = q_row0 + row;
-    float m_run = -INFINITY;   // running max of scale*log2e*s
-    float l_run = 0.f;         // running sum of exp2(.. - m_run)
+    const int q_abs = my_row0 + (threadIdx.x & 127);
+    float m_ref = -INFINITY;   // reference max (log2 domain) of p and l
+    float l_run = 0.f;         // sum of exp2(s*c - m_ref) over seen keys
     bool ok = true;
-    for (int j = 0; j < n_blocks; ++j) {
-      const int sb = j & 1;
+    for (int j = 0; j < nb; ++j) {
       // Warp-uniform outcome: the tcgen05 loads below are .sync.aligned.
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bSFull(sb), (j >> 1) & 1, wc))))
+      if (!(ok = __all_sync(0xffffffffu,
+                            mbar_wait(bSFull(x), j & 1, wc))))
         break;
       tc_fence_after();
       uint32_t sr[kBN];
-      const uint32_t s_addr = tmem + lane_off + (sb ? kColS1 : kColS0);
+      const uint32_t s_addr = tmem + lane_off + C::col_s(x);
 #pragma unroll
-      for (int cc = 0; cc < kBN / 32; ++cc) tmem_ld32(s_addr + cc * 32, sr + cc * 32);
+      for (int cc = 0; cc < kBN / 32; ++cc)
+        tmem_ld32(s_addr + cc * 32, sr + cc * 32);
       tmem_ld_wait();
 #pragma unroll
       for (int cc = 0; cc < kBN / 32; ++cc) reg_fence32(sr + cc * 32);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bSEmpty(sb));
 #define S_(i) __uint_as_float(sr[(i)])
 
       // ---- row extreme over the visible keys of this block ----
       const int col0 = j * kBN;
       const bool need_mask =
-          (col0 + kBN > p.Nkv) || (CAUSAL && col0 + kBN - 1 > q_row0);
+          (col0 + kBN > p.Nkv) || (CAUSAL && col0 + kBN - 1 > my_row0);
       int n_vis = kBN;   // keys [col0, col0 + n_vis) are visible to this row
       if (need_mask) {
         int lim = p.Nkv - col0;
@@ -265,21 +304,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float ext;
       if (!need_mask) {
-        float a0 = S_(0), a1 = S_(1), a2 = S_(2), a3 = S_(3);
+        float a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = S_(i);
         if (!neg_scale) {
 #pragma unroll
-          for (int i = 4; i < kBN; i += 4) {
-            a0 = fmaxf(a0, S_(i)); a1 = fmaxf(a1, S_(i + 1));
-            a2 = fmaxf(a2, S_(i + 2)); a3 = fmaxf(a3, S_(i + 3));
-          }
-          ext = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+          for (int i = 8; i < kBN; i += 8)
+#pragma unroll
+            for (int u = 0; u < 8; ++u) a[u] = fmaxf(a[u], S_(i + u));
+          ext = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])),
+                      fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
         } else {
 #pragma unroll
-          for (int i = 4; i < kBN; i += 4) {
-            a0 = fminf(a0, S_(i)); a1 = fminf(a1, S_(i + 1));
-            a2 = fminf(a2, S_(i + 2)); a3 = fminf(a3, S_(i + 3));
-          }
-          ext = fminf(fminf(a0, a1), fminf(a2, a3));
+          for (int i = 8; i < kBN; i += 8)
+#pragma unroll
+            for (int u = 0; u < 8; ++u) a[u] = fminf(a[u], S_(i + u));
+          ext = fminf(fminf(fminf(a[0], a[1]), fminf(a[2], a[3])),
+                      fminf(fminf(a[4], a[5]), fminf(a[6], a[7])));
         }
       } else {
         ext = neg_scale ? INFINITY : -INFINITY;
@@ -289,21 +330,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float m_blk = (n_vis > 0) ? ext * c : -INFINITY;
-      const float m_new = fmaxf(m_run, m_blk);
-      // exp2 base: finite whenever some key has been visible so far
+      // Move the reference max only when this block exceeds it by more than
+      // the threshold (always on the first visible block).
+      const bool move = m_blk > m_ref + kRescaleLog2 ||
+                        (m_ref == -INFINITY && m_blk != -INFINITY);
+      const float m_new = move ? m_blk : m_ref;
+      const float alpha =
+          (move && m_ref != -INFINITY) ? ex2_approx(m_ref - m_new) : 1.f;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - m_use);
 
       // ---- P = exp2(s * c - m), row sum, pack to bf16 ----
       uint32_t pp[kBN / 2];
-      float r0 = 0.f, r1 = 0.f;
+      float r[4] = {0.f, 0.f, 0.f, 0.f};
       if (!need_mask) {
 #pragma unroll
         for (int i = 0; i < kBN; i += 2) {
           const float e0 = ex2_approx(fmaf(S_(i), c, -m_use));
           const float e1 = ex2_approx(fmaf(S_(i + 1), c, -m_use));
-          r0 += e0;
-          r1 += e1;
+          r[(i >> 1) & 3] += e0 + e1;
           pp[i / 2] = pack_bf16x2(e0, e1);
         }
       } else {
@@ -312,48 +356,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float e0 = (i < n_vis) ? ex2_approx(fmaf(S_(i), c, -m_use)) : 0.f;
           const float e1 =
               (i + 1 < n_vis) ? ex2_approx(fmaf(S_(i + 1), c, -m_use)) : 0.f;
-          r0 += e0;
-          r1 += e1;
+          r[(i >> 1) & 3] += e0 + e1;
           pp[i / 2] = pack_bf16x2(e0, e1);
         }
       }
-      l_run = l_run * alpha + (r0 + r1);
 #undef S_
+      l_run = l_run * alpha + ((r[0] + r[1]) + (r[2] + r[3]));
+      m_ref = m_new;
 
-      // ---- O correction (needs PV_{j-1} complete) ----
-      if (j >= 1) {
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(bODone, (j - 1) & 1, wc))))
-          break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          const uint32_t o_addr = tmem + lane_off + kColO;
+      // ---- rescale O when the reference max moved.  S_x(j) complete means
+      // every earlier MMA of this thread, including PV_x(j-1), is complete,
+      // so O_x is stable here. ----
+      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        const uint32_t o_addr = tmem + lane_off + C::col_o(x);
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t orr[32];
-            tmem_ld32(o_addr + cc * 32, orr);
-            tmem_ld_wait();
-            reg_fence32(orr);
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t orr[32];
+          tmem_ld32(o_addr + cc * 32, orr);
+          tmem_ld_wait();
+          reg_fence32(orr);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-            tmem_st32(o_addr + cc * 32, orr);
-          }
+          for (int i = 0; i < 32; ++i)
+            orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+          tmem_st32(o_addr + cc * 32, orr);
         }
       }
-      const uint32_t p_addr = tmem + lane_off + (sb ? kColP1 : kColP0);
+      const uint32_t p_addr = tmem + lane_off + C::col_p(x);
       tmem_st32(p_addr, pp);
       tmem_st32(p_addr + 32, pp + 32);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bPFull);
-      m_run = m_new;
+      if (lane == 0) mbar_arrive(bPFull(x));
     }
 
     // ---- epilogue: O / l -> bf16, LSE ----
-    if (ok)
-      ok = __all_sync(0xffffffffu, mbar_wait(bODone, (n_blocks - 1) & 1, wc));
-    if (ok) {
+    if (ok && nb > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(bOFinal, 0, wc));
+    if (ok && nb > 0) {
       tc_fence_after();
       const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
       const bool in_range = q_abs < p.Nq;
@@ -361,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           (static_cast<size_t>(b) * p.Hq + hq) * static_cast<size_t>(p.Nq) +
           static_cast<size_t>(q_abs);
       __nv_bfloat16* orow = p.o + row_idx * D;
-      const uint32_t o_addr = tmem + lane_off + kColO;
+      const uint32_t o_addr = tmem + lane_off + C::col_o(x);
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t orr[32];
@@ -382,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (in_range && p.lse != nullptr) {
-        const float lse2 = (l_run > 0.f) ? (m_run + log2f(l_run)) : -INFINITY;
+        const float lse2 = (l_run > 0.f) ? (m_ref + log2f(l_run)) : -INFINITY;
         p.lse[row_idx] = lse2 * 0.69314718055994530942f;
       }
     }
