@@ -13,16 +13,19 @@
 // One CTA owns two 128-row query tiles (A: rows r0..r0+127, B: the next 128
 // rows) of one (batch, query head); both share every K/V block the CTA
 // loads.  Warp roles (320 threads):
-//   warps 0-3  softmax of tile A: thread t owns query row r0+t (TMEM lane t)
-//   warps 4-7  softmax of tile B (same lanes, its own TMEM columns)
+//   warp 0     MMA issuer (one thread), see below
+//   warp 1     TMA producer, see below
+//   warps 2-5  softmax of tile A: warp w owns rows 32*(w%4) .. +31 of the
+//              tile (its TMEM lane quadrant), one row per thread
+//   warps 6-9  softmax of tile B (same lanes, its own TMEM columns)
 //              each reads S from TMEM, masks the causal diagonal / ragged
 //              tail, keeps the row's reference max m and sum l in the log2
 //              domain (scale folded into one FFMA), writes P = exp2(s*c - m)
 //              as bf16 into TMEM, rescales its O accumulator in TMEM when m
 //              moves, and finally writes O / l and the LSE.
-//   warp 8     TMA producer: Q_A and Q_B once, then K_j and V_j into two
-//              rings of shared-memory stages (128-byte swizzle).
-//   warp 9     MMA issuer (one thread), in the order
+//   TMA producer: Q_A and Q_B once, then K_j and V_j into two rings of
+//              shared-memory stages (128-byte swizzle).
+//   MMA issuer (one thread), in the order
 //                 PV_A(j-1), S_A(j), PV_B(j-1), S_B(j), PV_A(j), ...
 //              so the tensor pipe works on one tile while the other tile's
 //              softmax runs.  S = Q K^T has both operands in shared memory
@@ -52,8 +55,11 @@ constexpr int kTilesPerCta = 2;
 constexpr int kBoxCols = 64;      // bf16 elements per 128-byte swizzle row
 constexpr int kBoxBytes = kBM * kBoxCols * 2;   // one TMA box: 128 x 64 bf16
 constexpr int kThreads = 320;
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
+// The MMA and TMA warps come first: the warp schedulers favour older warps,
+// and the single MMA-issuing thread must not queue behind the softmax warps.
+constexpr int kMmaWarp = 0;
+constexpr int kLoadWarp = 1;
+constexpr int kSoftmaxWarp0 = 2;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr uint32_t kTmemCols = 512;
 
@@ -62,14 +68,18 @@ struct FwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr int kTileBytes = kBM * D * 2;       // 16 KiB or 32 KiB
   static constexpr int kBoxes = D / kBoxCols;          // TMA boxes per tile
-  static constexpr int kStages = (D == 128) ? 2 : 4;   // K and V ring depth
+  // Ring depths.  V_j is released one MMA group later than K_j (after the
+  // second tile's P*V rather than its S), so V gets the deeper ring: both
+  // loads are then issued two iterations ahead of their use.
+  static constexpr int kKStages = (D == 128) ? 2 : 4;
+  static constexpr int kVStages = (D == 128) ? 3 : 4;
   // barriers: Q, K full/empty, V full/empty, S full x2, P full x2, O final,
   // drain
-  static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 1 + 1;
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1 + 1;
   static constexpr int kBarBytes = 8 * kNumBars + 16;  // + tmem slot + abort
   static constexpr int kSmemBytes =
-      1024 /*alignment slack*/ + kTileBytes * (kTilesPerCta + 2 * kStages) +
-      kBarBytes;
+      1024 /*alignment slack*/ +
+      kTileBytes * (kTilesPerCta + kKStages + kVStages) + kBarBytes;
   // TMEM column of tile x's S, O and P.
   __host__ __device__ static constexpr uint32_t col_s(int x) {
     return x ? 128u : 0u;
@@ -93,6 +103,38 @@ struct FwdParams {
   uint64_t wait_limit_ns;
 };
 
+// S = Q K^T for one tile and one K/V block: D/16 MMAs of 128x128x16.  Both
+// operands are K-major with the 128-byte swizzle; stepping K by 16 elements
+// moves the start address 32 bytes within a swizzle row, and every 64
+// elements to the next TMA box.  Offsets are compile-time constants added to
+// the start-address field of prebuilt descriptors.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dq,
+                                         uint64_t dk, uint32_t idesc) {
+  mma_ss_c<0>(d_tmem, dq, dk, idesc);
+#pragma unroll
+  for (int kk = 1; kk < D / 16; ++kk) {
+    const uint64_t off = static_cast<uint64_t>(
+        ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+    mma_ss_c<1>(d_tmem, dq + off, dk + off, idesc);
+  }
+}
+
+// O += P V for one tile and one K/V block: 8 MMAs of 128xDx16.  P (bf16x2
+// packed, 8 TMEM columns per 16 keys) comes from TMEM; V is MN-major with the
+// 128-byte swizzle, 16 keys = 2048 bytes per step.  `acc` is false for the
+// first block of a tile (initialises O).
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t a_tmem,
+                                         uint64_t dv, uint32_t idesc,
+                                         bool acc) {
+  mma_ts(d_tmem, a_tmem, dv, idesc, acc ? 1u : 0u);
+#pragma unroll
+  for (int kk = 1; kk < kBN / 16; ++kk)
+    mma_ts_c<1>(d_tmem, a_tmem + kk * 8,
+                dv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc);
+}
+
 // Number of K/V blocks a tile starting at query row `row0` visits.
 template <bool CAUSAL>
 __device__ __forceinline__ int kv_blocks(int row0, int Nkv) {
@@ -107,7 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmV,
                   const FwdParams p) {
   using C = FwdCfg<D>;
-  constexpr int NS = C::kStages;
+  constexpr int NK = C::kKStages;
+  constexpr int NV = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
 
   const int warp = threadIdx.x >> 5;
@@ -131,27 +174,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* const base_ptr = smem_raw + (base - smem_addr(smem_raw));
   const uint32_t sQ = base;                          // Q_A, then Q_B
   const uint32_t sK = sQ + kTilesPerCta * C::kTileBytes;
-  const uint32_t sV = sK + NS * C::kTileBytes;
-  const uint32_t sBar = sV + NS * C::kTileBytes;
+  const uint32_t sV = sK + NK * C::kTileBytes;
+  const uint32_t sBar = sV + NV * C::kTileBytes;
   auto bar = [&](int i) { return sBar + 8u * static_cast<uint32_t>(i); };
   const uint32_t bQFull = bar(0);
+  constexpr int kB0 = 1 + 2 * NK + 2 * NV;       // first non-ring barrier
   auto bKFull = [&](int s) { return bar(1 + s); };
-  auto bKEmpty = [&](int s) { return bar(1 + NS + s); };
-  auto bVFull = [&](int s) { return bar(1 + 2 * NS + s); };
-  auto bVEmpty = [&](int s) { return bar(1 + 3 * NS + s); };
-  auto bSFull = [&](int x) { return bar(1 + 4 * NS + x); };
-  auto bPFull = [&](int x) { return bar(3 + 4 * NS + x); };
-  const uint32_t bOFinal = bar(5 + 4 * NS);
-  const uint32_t bDrain = bar(6 + 4 * NS);
+  auto bKEmpty = [&](int s) { return bar(1 + NK + s); };
+  auto bVFull = [&](int s) { return bar(1 + 2 * NK + s); };
+  auto bVEmpty = [&](int s) { return bar(1 + 2 * NK + NV + s); };
+  auto bSFull = [&](int x) { return bar(kB0 + x); };
+  auto bPFull = [&](int x) { return bar(kB0 + 2 + x); };
+  const uint32_t bOFinal = bar(kB0 + 4);
+  const uint32_t bDrain = bar(kB0 + 5);
   uint8_t* const misc = base_ptr + (sBar - base) + 8 * C::kNumBars;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile uint32_t* const abort = reinterpret_cast<uint32_t*>(misc + 4);
 
   if (threadIdx.x == 0) {
     mbar_init(bQFull, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < NK; ++s) {
       mbar_init(bKFull(s), 1);
       mbar_init(bKEmpty(s), 1);
+    }
+    for (int s = 0; s < NV; ++s) {
       mbar_init(bVFull(s), 1);
       mbar_init(bVEmpty(s), 1);
     }
@@ -164,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort = 0u;
     mbar_init_fence();
   }
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -191,67 +237,61 @@ __global__ void __launch_bounds__(kThreads, 1)
                       c * kBoxCols, row0[x], zq, once);
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_blocks; ++j) {
-        const int s = j % NS;
-        const uint32_t ph = ((j / NS) & 1) ^ 1;
-        if (!mbar_wait(bKEmpty(s), ph, wc)) break;
-        mbar_arrive_expect_tx(bKFull(s), C::kTileBytes);
+        const int sk = j % NK, sv = j % NV;
+        if (!mbar_wait(bKEmpty(sk), ((j / NK) & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(bKFull(sk), C::kTileBytes);
         for (int c = 0; c < C::kBoxes; ++c)
-          tma_load_3d(sK + s * C::kTileBytes + c * kBoxBytes, &tmK, bKFull(s),
-                      c * kBoxCols, j * kBN, zk, keep);
+          tma_load_3d(sK + sk * C::kTileBytes + c * kBoxBytes, &tmK,
+                      bKFull(sk), c * kBoxCols, j * kBN, zk, keep);
         k_issued = j + 1;
-        if (!mbar_wait(bVEmpty(s), ph, wc)) break;
-        mbar_arrive_expect_tx(bVFull(s), C::kTileBytes);
+        if (!mbar_wait(bVEmpty(sv), ((j / NV) & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(bVFull(sv), C::kTileBytes);
         for (int c = 0; c < C::kBoxes; ++c)
-          tma_load_3d(sV + s * C::kTileBytes + c * kBoxBytes, &tmV, bVFull(s),
-                      c * kBoxCols, j * kBN, zk, keep);
+          tma_load_3d(sV + sv * C::kTileBytes + c * kBoxBytes, &tmV,
+                      bVFull(sv), c * kBoxCols, j * kBN, zk, keep);
         v_issued = j + 1;
       }
       // Never leave the CTA with copies in flight: wait (bounded) for the
       // last load issued into each stage of each ring, and for Q.
-      for (int j = (k_issued > NS ? k_issued - NS : 0); j < k_issued; ++j)
-        mbar_wait(bKFull(j % NS), (j / NS) & 1, wc, false);
-      for (int j = (v_issued > NS ? v_issued - NS : 0); j < v_issued; ++j)
-        mbar_wait(bVFull(j % NS), (j / NS) & 1, wc, false);
+      for (int j = (k_issued > NK ? k_issued - NK : 0); j < k_issued; ++j)
+        mbar_wait(bKFull(j % NK), (j / NK) & 1, wc, false);
+      for (int j = (v_issued > NV ? v_issued - NV : 0); j < v_issued; ++j)
+        mbar_wait(bVFull(j % NV), (j / NV) & 1, wc, false);
       mbar_wait(bQFull, 0, wc, false);
     }
   } else if (warp == kMmaWarp) {
     // ============================ MMA issuer ==============================
     if (lane == 0) {
+      // Descriptors of every operand tile, built once.
+      const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dK = sdesc_sw128(sK, 16, 1024);
+      const uint64_t dV = sdesc_sw128(sV, kBoxBytes, 1024);
+      constexpr uint64_t kStep = static_cast<uint64_t>(C::kTileBytes >> 4);
       bool ok = mbar_wait(bQFull, 0, wc);
       for (int j = 0; ok && j <= n_blocks; ++j) {
-        const int s = j % NS;
-        const int sp = (j + NS - 1) % NS;      // stage of block j-1
-        if (j < n_blocks && !(ok = mbar_wait(bKFull(s), (j / NS) & 1, wc)))
-          break;
+        const int s = j % NK;                  // K stage of block j
+        const int sp = (j + NV - 1) % NV;      // V stage of block j-1
         if (j >= 1 &&
-            !(ok = mbar_wait(bVFull(sp), ((j - 1) / NS) & 1, wc)))
+            !(ok = mbar_wait(bVFull(sp), ((j - 1) / NV) & 1, wc)))
           break;
+        if (j < n_blocks && !(ok = mbar_wait(bKFull(s), (j / NK) & 1, wc)))
+          break;
+        const uint64_t dKs = dK + static_cast<uint64_t>(s) * kStep;
+        const uint64_t dVs = dV + static_cast<uint64_t>(sp) * kStep;
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           // O_x += P_x(j-1) V_{j-1}
           if (j >= 1 && j - 1 < nblk[x]) {
             if (!(ok = mbar_wait(bPFull(x), (j - 1) & 1, wc))) break;
             tc_fence_after();
-            const uint32_t a_p = tmem + C::col_p(x);
-            const uint32_t v_base = sV + sp * C::kTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-              mma_ts(tmem + C::col_o(x), a_p + kk * 8,
-                     sdesc_sw128(v_base + kk * 2048, kBoxBytes, 1024),
-                     C::kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
+            issue_pv<D>(tmem + C::col_o(x), tmem + C::col_p(x), dVs,
+                        C::kIdescPV, j > 1);
           }
           // S_x(j) = Q_x K_j^T
           if (j < nblk[x]) {
-            tc_fence_after();
-            const uint32_t q_base = sQ + x * C::kTileBytes;
-            const uint32_t k_base = sK + s * C::kTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-              mma_ss(tmem + C::col_s(x), sdesc_sw128(q_base + off, 16, 1024),
-                     sdesc_sw128(k_base + off, 16, 1024), C::kIdescS,
-                     kk > 0 ? 1u : 0u);
-            }
+            issue_qk<D>(tmem + C::col_s(x),
+                        dQ + static_cast<uint64_t>(x) * kStep, dKs,
+                        C::kIdescS);
             mma_commit(bSFull(x));
           }
         }
@@ -266,13 +306,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ============================ softmax warps ===========================
-    const int x = warp >> 2;                       // tile A (0) or B (1)
+    const int x = (warp - kSoftmaxWarp0) >> 2;     // tile A (0) or B (1)
     const int nb = x ? nblk[1] : nblk[0];
     const int my_row0 = x ? row0[1] : row0[0];
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float c = p.scale_log2;
     const bool neg_scale = c < 0.f;
-    const int q_abs = my_row0 + (threadIdx.x & 127);
+    // TMEM lane quadrant of a warp is fixed by warp % 4.
+    const int q_abs = my_row0 + (warp & 3) * 32 + lane;
     float m_ref = -INFINITY;   // reference max (log2 domain) of p and l
     float l_run = 0.f;         // sum of exp2(s*c - m_ref) over seen keys
     bool ok = true;
@@ -304,23 +345,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float ext;
       if (!need_mask) {
+        // 8 independent chains over columns u, u+8, ..., u+120
         float a[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a[i] = S_(i);
         if (!neg_scale) {
 #pragma unroll
-          for (int i = 8; i < kBN; i += 8)
+          for (int u = 0; u < 8; ++u) {
+            float m = fmax3(S_(u), S_(u + 8), S_(u + 16));
 #pragma unroll
-            for (int u = 0; u < 8; ++u) a[u] = fmaxf(a[u], S_(i + u));
-          ext = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])),
-                      fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
+            for (int i = 24; i < kBN - 8; i += 16)
+              m = fmax3(m, S_(i + u), S_(i + 8 + u));
+            a[u] = fmaxf(m, S_(kBN - 8 + u));
+          }
+          ext = fmaxf(fmax3(fmax3(a[0], a[1], a[2]), a[3], a[4]),
+                      fmax3(a[5], a[6], a[7]));
         } else {
 #pragma unroll
-          for (int i = 8; i < kBN; i += 8)
+          for (int u = 0; u < 8; ++u) {
+            float m = fmin3(S_(u), S_(u + 8), S_(u + 16));
 #pragma unroll
-            for (int u = 0; u < 8; ++u) a[u] = fminf(a[u], S_(i + u));
-          ext = fminf(fminf(fminf(a[0], a[1]), fminf(a[2], a[3])),
-                      fminf(fminf(a[4], a[5]), fminf(a[6], a[7])));
+            for (int i = 24; i < kBN - 8; i += 16)
+              m = fmin3(m, S_(i + u), S_(i + 8 + u));
+            a[u] = fminf(m, S_(kBN - 8 + u));
+          }
+          ext = fminf(fmin3(fmin3(a[0], a[1], a[2]), a[3], a[4]),
+                      fmin3(a[5], a[6], a[7]));
         }
       } else {
         ext = neg_scale ? INFINITY : -INFINITY;
@@ -341,16 +389,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---- P = exp2(s * c - m), row sum, pack to bf16 ----
       uint32_t pp[kBN / 2];
-      float r[4] = {0.f, 0.f, 0.f, 0.f};
+      float rsum;
       if (!need_mask) {
+        // x = s*c - m on packed pairs (f32x2 FMA), exp2 on the MUFU, packed
+        // row sums, bf16x2 packing of P.
+        const uint64_t c2 = f2(c, c);
+        const uint64_t nm2 = f2(-m_use, -m_use);
+        uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int i = 0; i < kBN; i += 2) {
-          const float e0 = ex2_approx(fmaf(S_(i), c, -m_use));
-          const float e1 = ex2_approx(fmaf(S_(i + 1), c, -m_use));
-          r[(i >> 1) & 3] += e0 + e1;
+          float x0, x1;
+          f2_split(fma2(f2(S_(i), S_(i + 1)), c2, nm2), x0, x1);
+          const float e0 = ex2_approx(x0);
+          const float e1 = ex2_approx(x1);
+          acc[(i >> 1) & 3] = add2(acc[(i >> 1) & 3], f2(e0, e1));
           pp[i / 2] = pack_bf16x2(e0, e1);
         }
+        float s0, s1;
+        f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), s0, s1);
+        rsum = s0 + s1;
       } else {
+        float r[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < kBN; i += 2) {
           const float e0 = (i < n_vis) ? ex2_approx(fmaf(S_(i), c, -m_use)) : 0.f;
@@ -359,9 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           r[(i >> 1) & 3] += e0 + e1;
           pp[i / 2] = pack_bf16x2(e0, e1);
         }
+        rsum = (r[0] + r[1]) + (r[2] + r[3]);
       }
 #undef S_
-      l_run = l_run * alpha + ((r[0] + r[1]) + (r[2] + r[3]));
+      l_run = l_run * alpha + rsum;
       m_ref = m_new;
 
       // ---- rescale O when the reference max moved.  S_x(j) complete means
@@ -433,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace fa
