@@ -325,18 +325,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint32_t sr[kBN];
       const uint32_t s_addr = tmem + lane_off + C::col_s(x);
-#pragma unroll
-      for (int cc = 0; cc < kBN / 32; ++cc)
-        tmem_ld32(s_addr + cc * 32, sr + cc * 32);
-      tmem_ld_wait();
-#pragma unroll
-      for (int cc = 0; cc < kBN / 32; ++cc) reg_fence32(sr + cc * 32);
-#define S_(i) __uint_as_float(sr[(i)])
-
-      // ---- row extreme over the visible keys of this block ----
       const int col0 = j * kBN;
       const bool need_mask =
           (col0 + kBN > p.Nkv) || (CAUSAL && col0 + kBN - 1 > my_row0);
+      // Unmasked blocks take the row's extreme from reducing TMEM loads (one
+      // max/min per 32 columns, computed by the load itself).
+      float red[kBN / 32];
+      if (!need_mask && !neg_scale) {
+#pragma unroll
+        for (int cc = 0; cc < kBN / 32; ++cc)
+          tmem_ld32_max(s_addr + cc * 32, sr + cc * 32, red[cc]);
+      } else if (!need_mask) {
+#pragma unroll
+        for (int cc = 0; cc < kBN / 32; ++cc)
+          tmem_ld32_min(s_addr + cc * 32, sr + cc * 32, red[cc]);
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < kBN / 32; ++cc) {
+          tmem_ld32(s_addr + cc * 32, sr + cc * 32);
+          red[cc] = 0.f;
+        }
+      }
+      tmem_ld_wait();
+#pragma unroll
+      for (int cc = 0; cc < kBN / 32; ++cc) {
+        reg_fence32(sr + cc * 32);
+        reg_fence_f(red[cc]);
+      }
+#define S_(i) __uint_as_float(sr[(i)])
+
+      // ---- row extreme over the visible keys of this block ----
       int n_vis = kBN;   // keys [col0, col0 + n_vis) are visible to this row
       if (need_mask) {
         int lim = p.Nkv - col0;
@@ -345,31 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float ext;
       if (!need_mask) {
-        // 8 independent chains over columns u, u+8, ..., u+120
-        float a[8];
-        if (!neg_scale) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            float m = fmax3(S_(u), S_(u + 8), S_(u + 16));
-#pragma unroll
-            for (int i = 24; i < kBN - 8; i += 16)
-              m = fmax3(m, S_(i + u), S_(i + 8 + u));
-            a[u] = fmaxf(m, S_(kBN - 8 + u));
-          }
-          ext = fmaxf(fmax3(fmax3(a[0], a[1], a[2]), a[3], a[4]),
-                      fmax3(a[5], a[6], a[7]));
-        } else {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            float m = fmin3(S_(u), S_(u + 8), S_(u + 16));
-#pragma unroll
-            for (int i = 24; i < kBN - 8; i += 16)
-              m = fmin3(m, S_(i + u), S_(i + 8 + u));
-            a[u] = fminf(m, S_(kBN - 8 + u));
-          }
-          ext = fminf(fmin3(fmin3(a[0], a[1], a[2]), a[3], a[4]),
-                      fmin3(a[5], a[6], a[7]));
-        }
+        ext = neg_scale ? fminf(fminf(red[0], red[1]), fminf(red[2], red[3]))
+                        : fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
       } else {
         ext = neg_scale ? INFINITY : -INFINITY;
 #pragma unroll
