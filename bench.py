@@ -66,6 +66,25 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x, device="cpu"):
+    """Largest value of ``x`` over all ranks of the default process group
+    (``x`` itself without one).  NCCL needs ``device`` to be the rank's GPU;
+    gloo works on the CPU."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or \
+            dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank, ms_slowest, world_size):
+    """Whole-job throughput: every rank's work over the slowest rank's time
+    (each rank runs its own replica of the workload: weak scaling)."""
+    return world_size * flops_per_rank / (ms_slowest * 1e-3) / 1e12
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -158,30 +177,30 @@ class ClockSampler:
 
 
 def cpu_baseline(w, q, k, v, seconds):
-    """The oracle as it stands, on this host's cores, on whole heads of the
-    workload until about ``seconds`` of CPU work (at least one head)."""
+    """The oracle as it stands, on this host's cores, over (batch, head)
+    slices of the workload (repeating the workload if it is short) until
+    about ``seconds`` of CPU work (at least one slice)."""
     import oracle
     cores = len(os.sched_getaffinity(0))
     torch.set_num_threads(cores)
     group = w.Hq // w.Hkv
+    slices = [(b, h) for b in range(w.B) for h in range(w.Hq)]
     t0 = time.perf_counter()
-    heads = 0
-    for b in range(w.B):
-        for h in range(w.Hq):
-            hk = h // group
-            oracle.attention_fp64(q[b:b + 1, h:h + 1], k[b:b + 1, hk:hk + 1],
-                                  v[b:b + 1, hk:hk + 1], w.scale, w.causal)
-            heads += 1
-            if time.perf_counter() - t0 >= seconds:
-                break
+    done = 0
+    while True:
+        b, h = slices[done % len(slices)]
+        hk = h // group
+        oracle.attention_fp64(q[b:b + 1, h:h + 1], k[b:b + 1, hk:hk + 1],
+                              v[b:b + 1, hk:hk + 1], w.scale, w.causal)
+        done += 1
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    flops = w.flops / (w.B * w.Hq) * heads
+    flops = w.flops / len(slices) * done
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores,
             "kind": "oracle",
-            "sample": f"{heads} of {w.B * w.Hq} (batch, head) slices of "
-                      f"{w.name}, float64, {dt:.1f} s"}
+            "sample": f"{done} (batch, head) slices of {w.name} "
+                      f"({len(slices)} per workload), float64, {dt:.1f} s"}
 
 
 def run_reference(args, w):
@@ -285,12 +304,8 @@ def run_ours(args, w):
         raise RuntimeError("bounded-wait timeout during the timed loop")
     per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(per) / len(per)
-    ms_max = ms
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(t.item())
-    value = ws * w.flops / (ms_max * 1e-3) / 1e12
+    ms_max = max_over_ranks(ms, dev)
+    value = job_tflops(w.flops, ms_max, ws)
     per_launch_tflops = w.flops / (ms * 1e-3) / 1e12
     peak, peak_src = peaks()
 
@@ -305,11 +320,7 @@ def run_ours(args, w):
     for _ in range(e2e_steps):
         fa.fwd_host(qp, kp, vp, scale=w.scale, causal=w.causal, bufs=bufs)
     barrier()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if ws > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, dev)
     h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
 
@@ -343,7 +354,7 @@ def run_ours(args, w):
                      "kernel": "fa_fwd_kernel",
                      "algorithmic_flops_per_launch": w.flops},
         "cpu_baseline": cpu,
-        "e2e": {"value": w.flops * ws / e2e_s / 1e12, "unit": UNIT,
+        "e2e": {"value": job_tflops(w.flops, e2e_s * 1e3, ws), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s * 1e3},
         "gpu_launches": args.steps,
