@@ -50,17 +50,23 @@ EncodeTiledFn encode_fn() {
 
 template <int D, bool CAUSAL>
 cudaError_t opt_in_smem() {
-  return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL>,
+  cudaError_t e = cudaFuncSetAttribute(
+      fa::fa_fwd_kernel<D, CAUSAL, false>,
+      cudaFuncAttributeMaxDynamicSharedMemorySize, fa::FwdCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               fa::FwdCfg<D>::kSmemBytes);
 }
 
 int* g_status_word[kMaxDevices];
+int g_sm_count[kMaxDevices];
+cudaMemPool_t g_pool[kMaxDevices];
 
 // Per-device readiness: compute capability 10.3, the kernels' shared memory
 // opt-in and the device address of the status word, done once per device
 // with that device current.
-int device_ready(int** word_out) {
+int device_ready(int** word_out, int* dev_out = nullptr) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
@@ -93,10 +99,59 @@ int device_ready(int** word_out) {
       return;
     }
     g_status_word[dev] = static_cast<int*>(word);
+    if (cudaDeviceGetAttribute(&g_sm_count[dev],
+                               cudaDevAttrMultiProcessorCount,
+                               dev) != cudaSuccess)
+      return;
+    // Stream-ordered pool for fa_fwd's split-KV scratch (fa_fwd_ws takes
+    // the caller's memory instead); freed blocks stay cached in the pool.
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    uint64_t keep = ~0ull;
+    if (cudaMemPoolCreate(&g_pool[dev], &props) != cudaSuccess ||
+        cudaMemPoolSetAttribute(g_pool[dev], cudaMemPoolAttrReleaseThreshold,
+                                &keep) != cudaSuccess)
+      return;
     status[dev] = FA_OK;
   });
   if (status[dev] == FA_OK && word_out != nullptr) *word_out = g_status_word[dev];
+  if (status[dev] == FA_OK && dev_out != nullptr) *dev_out = dev;
   return status[dev];
+}
+
+// Split-KV: when the pairs of query tiles fill fewer than half the SMs, cut
+// each pair's K/V range into contiguous pieces (at least kMinSplitBlocks
+// blocks each, at most kMaxSplits pieces) so about one CTA runs per SM.
+constexpr int kMinSplitBlocks = 4;
+constexpr int kMaxSplits = 64;
+
+int plan_splits(int B, int Hq, int Nq, int Nkv, int causal, int sms) {
+  const long long pairs = (Nq + fa::kBM * fa::kTilesPerCta - 1) /
+                          (fa::kBM * fa::kTilesPerCta);
+  const long long ctas = pairs * Hq * B;
+  if (ctas * 2 > sms) return 1;
+  int longest = (Nkv + fa::kBN - 1) / fa::kBN;           // K/V blocks
+  if (causal) {
+    const int rows = Nq < Nkv ? Nq : Nkv;
+    longest = (rows + fa::kBN - 1) / fa::kBN;
+  }
+  long long s = (sms + ctas - 1) / ctas;
+  const long long by_len = longest / kMinSplitBlocks;
+  if (s > by_len) s = by_len;
+  if (s > kMaxSplits) s = kMaxSplits;
+  if (s > 65535 / B) s = 65535 / B;                      // grid.z limit
+  return s < 1 ? 1 : static_cast<int>(s);
+}
+
+int64_t workspace_bytes(int B, int Hq, int Nq, int D, int splits) {
+  if (splits <= 1) return 0;
+  const int64_t pairs = (Nq + fa::kBM * fa::kTilesPerCta - 1) /
+                        (fa::kBM * fa::kTilesPerCta);
+  const int64_t slot = D == 64 ? fa::FwdCfg<64>::kSlotFloats
+                               : fa::FwdCfg<128>::kSlotFloats;
+  return static_cast<int64_t>(B) * Hq * pairs * splits * slot * 4;
 }
 
 // Tensor map of a contiguous bf16 [BH, N, D] tensor, read in 64 x 128 boxes
@@ -127,10 +182,24 @@ int launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
            const fa::FwdParams& p, int B, int Hq, int Nq,
            cudaStream_t stream) {
   const int rows_per_cta = fa::kBM * fa::kTilesPerCta;
-  dim3 grid((Nq + rows_per_cta - 1) / rows_per_cta, Hq, B);
-  fa::fa_fwd_kernel<D, CAUSAL>
-      <<<grid, fa::kThreads, fa::FwdCfg<D>::kSmemBytes, stream>>>(q, k, v, p);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  const int pairs = (Nq + rows_per_cta - 1) / rows_per_cta;
+  dim3 grid(pairs, Hq, B * p.kv_splits);
+  if (p.kv_splits > 1)
+    fa::fa_fwd_kernel<D, CAUSAL, true>
+        <<<grid, fa::kThreads, fa::FwdCfg<D>::kSmemBytes, stream>>>(q, k, v,
+                                                                     p);
+  else
+    fa::fa_fwd_kernel<D, CAUSAL, false>
+        <<<grid, fa::kThreads, fa::FwdCfg<D>::kSmemBytes, stream>>>(q, k, v,
+                                                                     p);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  if (p.kv_splits > 1) {
+    constexpr int kRowsPerBlock = 256 / (D / 4);
+    dim3 mgrid(pairs * (rows_per_cta / kRowsPerBlock), Hq, B);
+    fa::fa_merge_kernel<D><<<mgrid, 256, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return FA_OK;
 }
 
 bool aligned(const void* p, uintptr_t a) {
@@ -151,13 +220,9 @@ __global__ void probe_wait_kernel(int* status, uint64_t limit_ns) {
   __syncwarp();
 }
 
-}  // namespace
-
-extern "C" {
-
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-           int B, int Hq, int Hkv, int Nq, int Nkv, int D, float scale,
-           int causal, void* stream) {
+int check_args(const void* q, const void* k, const void* v, const void* o,
+               const float* lse, int B, int Hq, int Hkv, int Nq, int Nkv,
+               int D, float scale) {
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr)
     return FA_ERR_INVALID_VALUE;
   if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nkv < 1 || D < 1)
@@ -169,16 +234,20 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
       !aligned(o, 16) || (lse != nullptr && !aligned(lse, 4)))
     return FA_ERR_MISALIGNED;
+  return FA_OK;
+}
 
-  int* word = nullptr;
-  int st = device_ready(&word);
+// Shared body of fa_fwd and fa_fwd_ws.  Scratch: from the device pool when
+// `pool_scratch`, else the caller's `workspace` (`ws_bytes` long).
+int run_forward(const void* q, const void* k, const void* v, void* o,
+                float* lse, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                float scale, int causal, void* workspace, size_t ws_bytes,
+                bool pool_scratch, cudaStream_t s) {
+  int st = check_args(q, k, v, o, lse, B, Hq, Hkv, Nq, Nkv, D, scale);
   if (st != FA_OK) return st;
-
-  CUtensorMap tq, tk, tv;
-  if ((st = encode_bhnd(&tq, q, static_cast<long long>(B) * Hq, Nq, D)) ||
-      (st = encode_bhnd(&tk, k, static_cast<long long>(B) * Hkv, Nkv, D)) ||
-      (st = encode_bhnd(&tv, v, static_cast<long long>(B) * Hkv, Nkv, D)))
-    return st;
+  int* word = nullptr;
+  int dev = 0;
+  if ((st = device_ready(&word, &dev)) != FA_OK) return st;
 
   fa::FwdParams p;
   p.o = static_cast<__nv_bfloat16*>(o);
@@ -191,12 +260,77 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                                     1.4426950408889634074);
   p.status = word;
   p.wait_limit_ns = kWaitLimitNs;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  p.kv_splits = plan_splits(B, Hq, Nq, Nkv, causal, g_sm_count[dev]);
+  p.work = nullptr;
+  const int64_t need = workspace_bytes(B, Hq, Nq, D, p.kv_splits);
+  void* owned = nullptr;
+  if (need > 0) {
+    if (pool_scratch) {
+      if (cudaMallocFromPoolAsync(&owned, static_cast<size_t>(need),
+                                  g_pool[dev], s) != cudaSuccess)
+        return FA_ERR_CUDA;
+      p.work = static_cast<float*>(owned);
+    } else {
+      if (workspace == nullptr || ws_bytes < static_cast<size_t>(need))
+        return FA_ERR_INVALID_VALUE;
+      if (!aligned(workspace, 16)) return FA_ERR_MISALIGNED;
+      p.work = static_cast<float*>(workspace);
+    }
+  }
+
+  CUtensorMap tq, tk, tv;
+  if ((st = encode_bhnd(&tq, q, static_cast<long long>(B) * Hq, Nq, D)) ||
+      (st = encode_bhnd(&tk, k, static_cast<long long>(B) * Hkv, Nkv, D)) ||
+      (st = encode_bhnd(&tv, v, static_cast<long long>(B) * Hkv, Nkv, D))) {
+    if (owned != nullptr) cudaFreeAsync(owned, s);
+    return st;
+  }
   if (D == 64)
-    return causal ? launch<64, true>(tq, tk, tv, p, B, Hq, Nq, s)
-                  : launch<64, false>(tq, tk, tv, p, B, Hq, Nq, s);
-  return causal ? launch<128, true>(tq, tk, tv, p, B, Hq, Nq, s)
+    st = causal ? launch<64, true>(tq, tk, tv, p, B, Hq, Nq, s)
+                : launch<64, false>(tq, tk, tv, p, B, Hq, Nq, s);
+  else
+    st = causal ? launch<128, true>(tq, tk, tv, p, B, Hq, Nq, s)
                 : launch<128, false>(tq, tk, tv, p, B, Hq, Nq, s);
+  if (owned != nullptr && cudaFreeAsync(owned, s) != cudaSuccess &&
+      st == FA_OK)
+    st = FA_ERR_CUDA;
+  return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int Hq, int Hkv, int Nq, int Nkv, int D, float scale,
+           int causal, void* stream) {
+  return run_forward(q, k, v, o, lse, B, Hq, Hkv, Nq, Nkv, D, scale, causal,
+                     nullptr, 0, true, static_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd_ws(const void* q, const void* k, const void* v, void* o,
+              float* lse, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+              float scale, int causal, void* workspace,
+              size_t workspace_bytes_, void* stream) {
+  return run_forward(q, k, v, o, lse, B, Hq, Hkv, Nq, Nkv, D, scale, causal,
+                     workspace, workspace_bytes_, false,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                          int causal, size_t* bytes) {
+  if (bytes == nullptr) return FA_ERR_INVALID_VALUE;
+  *bytes = 0;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nkv < 1 || D < 1 ||
+      Hq % Hkv != 0 || B > 65535 || Hq > 65535)
+    return FA_ERR_INVALID_VALUE;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  int dev = 0;
+  const int st = device_ready(nullptr, &dev);
+  if (st != FA_OK) return st;
+  *bytes = static_cast<size_t>(workspace_bytes(
+      B, Hq, Nq, D, plan_splits(B, Hq, Nq, Nkv, causal, g_sm_count[dev])));
+  return FA_OK;
 }
 
 const char* fa_status_string(int status) {

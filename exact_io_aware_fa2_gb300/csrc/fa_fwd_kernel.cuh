@@ -92,6 +92,10 @@ struct FwdCfg {
   }
   static constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);
+  // fp32 words of one partial slot: O rows [256][D] (unnormalised, relative
+  // to the slot's reference max), then m[256] (log2 domain), then l[256].
+  static constexpr int64_t kSlotFloats =
+      static_cast<int64_t>(kTilesPerCta * kBM) * (D + 2);
 };
 
 struct FwdParams {
@@ -101,6 +105,11 @@ struct FwdParams {
   float scale_log2;   // scale * log2(e)
   int* status;        // device status word (bounded-wait timeouts)
   uint64_t wait_limit_ns;
+  // Split-KV: each (batch, head, tile pair) is cut into kv_splits contiguous
+  // ranges of K/V blocks, one CTA each.  With kv_splits > 1 the CTAs leave
+  // fp32 partials in `work` (see kSlotFloats) for fa_merge_kernel.
+  int kv_splits;
+  float* work;
 };
 
 // S = Q K^T for one tile and one K/V block: D/16 MMAs of 128x128x16.  Both
@@ -142,12 +151,15 @@ __device__ __forceinline__ int kv_blocks(int row0, int Nkv) {
   return (end + kBN - 1) / kBN;
 }
 
-template <int D, bool CAUSAL>
+// SPLIT: the grid's z index also carries the K/V range (split-KV) and the
+// epilogue writes fp32 partials; without it the code is the plain one-pair-
+// per-CTA forward.
+template <int D, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV,
-                  const FwdParams p) {
+                  const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   constexpr int NK = C::kKStages;
   constexpr int NV = C::kVStages;
@@ -161,13 +173,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pair = CAUSAL ? (n_pairs - 1 - static_cast<int>(blockIdx.x))
                           : static_cast<int>(blockIdx.x);
   const int hq = blockIdx.y;
-  const int b = blockIdx.z;
+  const int splits = SPLIT ? p.kv_splits : 1;
+  const int b = SPLIT ? static_cast<int>(blockIdx.z) / splits
+                      : static_cast<int>(blockIdx.z);
+  const int split = SPLIT ? static_cast<int>(blockIdx.z) - b * splits : 0;
   const int hk = hq / (p.Hq / p.Hkv);
   const int row0[2] = {pair * (2 * kBM), pair * (2 * kBM) + kBM};
   const bool has_b = row0[1] < p.Nq;
   const int nblk[2] = {kv_blocks<CAUSAL>(row0[0], p.Nkv),
                        has_b ? kv_blocks<CAUSAL>(row0[1], p.Nkv) : 0};
-  const int n_blocks = max(nblk[0], nblk[1]);
+  // This CTA's contiguous range [j0, j1) of the pair's K/V blocks.  A tile
+  // visits the prefix [j0, min(j1, nblk)) of it (causal tiles end earlier).
+  const int n_pair = max(nblk[0], nblk[1]);
+  const int chunk = SPLIT ? (n_pair + splits - 1) / splits : n_pair;
+  const int j0 = SPLIT ? min(n_pair, split * chunk) : 0;
+  const int n_blocks = SPLIT ? min(n_pair, j0 + chunk) - j0 : n_pair;
 
   // ---- shared memory carve-up (1024-byte aligned for the swizzle atoms) --
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -236,20 +256,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sQ + x * C::kTileBytes + c * kBoxBytes, &tmQ, bQFull,
                       c * kBoxCols, row0[x], zq, once);
       int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < n_blocks; ++j) {
-        const int sk = j % NK, sv = j % NV;
-        if (!mbar_wait(bKEmpty(sk), ((j / NK) & 1) ^ 1, wc)) break;
+      for (int i = 0; i < n_blocks; ++i) {
+        const int j = j0 + i;                    // block index in the pair
+        const int sk = i % NK, sv = i % NV;
+        if (!mbar_wait(bKEmpty(sk), ((i / NK) & 1) ^ 1, wc)) break;
         mbar_arrive_expect_tx(bKFull(sk), C::kTileBytes);
         for (int c = 0; c < C::kBoxes; ++c)
           tma_load_3d(sK + sk * C::kTileBytes + c * kBoxBytes, &tmK,
                       bKFull(sk), c * kBoxCols, j * kBN, zk, keep);
-        k_issued = j + 1;
-        if (!mbar_wait(bVEmpty(sv), ((j / NV) & 1) ^ 1, wc)) break;
+        k_issued = i + 1;
+        if (!mbar_wait(bVEmpty(sv), ((i / NV) & 1) ^ 1, wc)) break;
         mbar_arrive_expect_tx(bVFull(sv), C::kTileBytes);
         for (int c = 0; c < C::kBoxes; ++c)
           tma_load_3d(sV + sv * C::kTileBytes + c * kBoxBytes, &tmV,
                       bVFull(sv), c * kBoxCols, j * kBN, zk, keep);
-        v_issued = j + 1;
+        v_issued = i + 1;
       }
       // Never leave the CTA with copies in flight: wait (bounded) for the
       // last load issued into each stage of each ring, and for Q.
@@ -268,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dV = sdesc_sw128(sV, kBoxBytes, 1024);
       constexpr uint64_t kStep = static_cast<uint64_t>(C::kTileBytes >> 4);
       bool ok = mbar_wait(bQFull, 0, wc);
+      // j counts this CTA's blocks (ring position); block j0 + j of the pair
       for (int j = 0; ok && j <= n_blocks; ++j) {
         const int s = j % NK;                  // K stage of block j
         const int sp = (j + NV - 1) % NV;      // V stage of block j-1
@@ -281,14 +303,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           // O_x += P_x(j-1) V_{j-1}
-          if (j >= 1 && j - 1 < nblk[x]) {
+          if (j >= 1 && j0 + j - 1 < nblk[x]) {
             if (!(ok = mbar_wait(bPFull(x), (j - 1) & 1, wc))) break;
             tc_fence_after();
             issue_pv<D>(tmem + C::col_o(x), tmem + C::col_p(x), dVs,
                         C::kIdescPV, j > 1);
           }
           // S_x(j) = Q_x K_j^T
-          if (j < nblk[x]) {
+          if (j < n_blocks && j0 + j < nblk[x]) {
             issue_qk<D>(tmem + C::col_s(x),
                         dQ + static_cast<uint64_t>(x) * kStep, dKs,
                         C::kIdescS);
@@ -307,7 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ============================ softmax warps ===========================
     const int x = (warp - kSoftmaxWarp0) >> 2;     // tile A (0) or B (1)
-    const int nb = x ? nblk[1] : nblk[0];
+    // blocks of this tile in the CTA's range: [j0, j0 + nb)
+    const int nb = max(0, min(j0 + n_blocks, x ? nblk[1] : nblk[0]) - j0);
     const int my_row0 = x ? row0[1] : row0[0];
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float c = p.scale_log2;
@@ -325,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint32_t sr[kBN];
       const uint32_t s_addr = tmem + lane_off + C::col_s(x);
-      const int col0 = j * kBN;
+      const int col0 = (j0 + j) * kBN;
       const bool need_mask =
           (col0 + kBN > p.Nkv) || (CAUSAL && col0 + kBN - 1 > my_row0);
       // Unmasked blocks take the row's extreme from reducing TMEM loads (one
@@ -445,7 +468,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bPFull(x));
     }
 
-    // ---- epilogue: O / l -> bf16, LSE ----
+    // ---- epilogue ----
+    if constexpr (SPLIT) {
+      // Partial of one K/V range: unnormalised O (relative to m_ref), m and
+      // l per row, for fa_merge_kernel.  A tile with no block in this range
+      // leaves l = 0, m = -inf.
+      float* slot = p.work + ((static_cast<int64_t>(b) * p.Hq + hq) *
+                                  static_cast<int64_t>(gridDim.x) +
+                              pair) * splits * C::kSlotFloats +
+                    static_cast<int64_t>(split) * C::kSlotFloats;
+      const int prow = q_abs - pair * (2 * kBM);     // row within the pair
+      if (ok && nb > 0)
+        ok = __all_sync(0xffffffffu, mbar_wait(bOFinal, 0, wc));
+      if (ok && nb > 0) {
+        tc_fence_after();
+        const uint32_t o_addr = tmem + lane_off + C::col_o(x);
+        float4* orow = reinterpret_cast<float4*>(slot + prow * D);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t orr[32];
+          tmem_ld32(o_addr + cc * 32, orr);
+          tmem_ld_wait();
+          reg_fence32(orr);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            orow[cc * 8 + i] = make_float4(
+                __uint_as_float(orr[4 * i]), __uint_as_float(orr[4 * i + 1]),
+                __uint_as_float(orr[4 * i + 2]),
+                __uint_as_float(orr[4 * i + 3]));
+        }
+      }
+      slot[kTilesPerCta * kBM * D + prow] = nb > 0 ? m_ref : -INFINITY;
+      slot[kTilesPerCta * kBM * D + kTilesPerCta * kBM + prow] =
+          nb > 0 ? l_run : 0.f;
+    } else {
     if (ok && nb > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(bOFinal, 0, wc));
     if (ok && nb > 0) {
@@ -481,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.lse[row_idx] = lse2 * 0.69314718055994530942f;
       }
     }
+    }
   }
 
   // ---- teardown: every role is done with TMEM and shared memory ----
@@ -489,6 +546,64 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Split-KV merge: for every query row, combine the partials of its K/V
+// ranges.  Range s left O_s (unnormalised, relative to its reference max
+// m_s, log2 domain) and l_s; with m = max_s m_s
+//     l = sum_s l_s 2^(m_s - m),   O = sum_s O_s 2^(m_s - m) / l,
+//     LSE = (m + log2 l) ln 2,
+// the same rescaling the online softmax applies between K/V blocks.  One
+// thread per (row, 4 columns); grid (pairs * 256 / rows-per-block, Hq, B).
+template <int D>
+__global__ void __launch_bounds__(256)
+    fa_merge_kernel(const __grid_constant__ FwdParams p) {
+  using C = FwdCfg<D>;
+  constexpr int kRows = kTilesPerCta * kBM;       // rows of a pair
+  constexpr int kChunks = D / 4;                  // float4 per row
+  constexpr int kRowsPerBlock = 256 / kChunks;
+  const int splits = p.kv_splits;
+  const int blocks_per_pair = kRows / kRowsPerBlock;
+  const int pair = static_cast<int>(blockIdx.x) / blocks_per_pair;
+  const int prow = (static_cast<int>(blockIdx.x) % blocks_per_pair) *
+                       kRowsPerBlock +
+                   static_cast<int>(threadIdx.x) / kChunks;
+  const int ch = static_cast<int>(threadIdx.x) % kChunks;
+  const int hq = blockIdx.y, b = blockIdx.z;
+  const int q_row = pair * kRows + prow;
+  if (q_row >= p.Nq) return;
+  const int n_pairs = (p.Nq + kRows - 1) / kRows;
+  const float* base = p.work + ((static_cast<int64_t>(b) * p.Hq + hq) *
+                                    n_pairs + pair) * splits * C::kSlotFloats;
+  float m = -INFINITY;
+  for (int s = 0; s < splits; ++s)
+    m = fmaxf(m, base[s * C::kSlotFloats + kRows * D + prow]);
+  float l = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int s = 0; s < splits; ++s) {
+    const float* slot = base + s * C::kSlotFloats;
+    const float ms = slot[kRows * D + prow];
+    if (ms == -INFINITY) continue;                // range saw no key
+    const float w = ex2_approx(ms - m);
+    l += slot[kRows * D + kRows + prow] * w;
+    const float4 o = reinterpret_cast<const float4*>(slot + prow * D)[ch];
+    acc.x += o.x * w;
+    acc.y += o.y * w;
+    acc.z += o.z * w;
+    acc.w += o.w * w;
+  }
+  const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+  const size_t row_idx =
+      (static_cast<size_t>(b) * p.Hq + hq) * static_cast<size_t>(p.Nq) +
+      static_cast<size_t>(q_row);
+  uint2 packed;
+  packed.x = pack_bf16x2(acc.x * inv_l, acc.y * inv_l);
+  packed.y = pack_bf16x2(acc.z * inv_l, acc.w * inv_l);
+  reinterpret_cast<uint2*>(p.o + row_idx * D)[ch] = packed;
+  if (ch == 0 && p.lse != nullptr)
+    p.lse[row_idx] =
+        (l > 0.f ? (m + log2f(l)) : -INFINITY) * 0.69314718055994530942f;
 }
 
 }  // namespace fa

@@ -27,7 +27,8 @@ FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_VALUE", 2: "FA_ERR_UNSUPPORTED",
                 3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
 # Every symbol the header declares.
-SYMBOLS = ("fa_fwd", "fa_status_string", "fa_last_device_error",
+SYMBOLS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size",
+           "fa_status_string", "fa_last_device_error",
            "fa_probe_bounded_wait", "fa_version")
 
 _lib = None
@@ -59,6 +60,12 @@ def load():
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci,
                                ctypes.c_float, ci, vp]
         lib.fa_fwd.restype = ci
+        lib.fa_fwd_ws.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci,
+                                  ctypes.c_float, ci, vp, ctypes.c_size_t, vp]
+        lib.fa_fwd_ws.restype = ci
+        lib.fa_fwd_workspace_size.argtypes = [
+            ci, ci, ci, ci, ci, ci, ci, ctypes.POINTER(ctypes.c_size_t)]
+        lib.fa_fwd_workspace_size.restype = ci
         lib.fa_status_string.argtypes = [ci]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_last_device_error.argtypes = []
@@ -109,9 +116,44 @@ def fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, Nq, Nkv, D,
         ctypes.c_void_p(stream_handle)))
 
 
+_ws_cache = {}
+
+
+def workspace_size(B, Hq, Hkv, Nq, Nkv, D, causal):
+    """Scratch bytes ``fa_fwd_ws`` needs for this shape (current device);
+    the answer depends only on the shape and the device, so it is cached."""
+    key = (torch.cuda.current_device(), B, Hq, Hkv, Nq, Nkv, D, bool(causal))
+    hit = _ws_cache.get(key)
+    if hit is not None:
+        return hit
+    n = ctypes.c_size_t(0)
+    st = int(load().fa_fwd_workspace_size(B, Hq, Hkv, Nq, Nkv, D,
+                                          1 if causal else 0,
+                                          ctypes.byref(n)))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_workspace_size")
+    _ws_cache[key] = int(n.value)
+    return int(n.value)
+
+
+def fwd_ws_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, Nq, Nkv, D,
+               scale, causal, ws_ptr, ws_bytes, stream_handle):
+    """Direct call of ``fa_fwd_ws`` with integer pointers; returns status."""
+    return int(load().fa_fwd_ws(
+        ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+        ctypes.c_void_p(o_ptr), ctypes.c_void_p(lse_ptr),
+        B, Hq, Hkv, Nq, Nkv, D, ctypes.c_float(scale), 1 if causal else 0,
+        ctypes.c_void_p(ws_ptr), ctypes.c_size_t(ws_bytes),
+        ctypes.c_void_p(stream_handle)))
+
+
 def fwd(q, k, v, scale=None, causal=False, out=None, lse=None,
-        want_lse=True):
-    """Attention forward through the C ABI on the current CUDA stream."""
+        want_lse=True, workspace=None):
+    """Attention forward through the C ABI on the current CUDA stream.
+
+    Split-KV scratch (only for shapes that need it) comes from
+    ``workspace`` (a uint8 CUDA tensor) or, if None, from torch's caching
+    allocator for this call."""
     B, Hq, Hkv, Nq, Nkv, D = _check(q, k, v)
     dev = q.device
     if dev.type != "cuda" or k.device != dev or v.device != dev:
@@ -123,10 +165,15 @@ def fwd(q, k, v, scale=None, causal=False, out=None, lse=None,
     if want_lse and lse is None:
         lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
+        need = workspace_size(B, Hq, Hkv, Nq, Nkv, D, causal)
+        if need > 0 and (workspace is None or workspace.numel() < need):
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         stream = torch.cuda.current_stream(dev).cuda_stream
-        st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                     lse.data_ptr() if lse is not None else 0,
-                     B, Hq, Hkv, Nq, Nkv, D, scale, causal, stream)
+        st = fwd_ws_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                        out.data_ptr(),
+                        lse.data_ptr() if lse is not None else 0,
+                        B, Hq, Hkv, Nq, Nkv, D, scale, causal,
+                        workspace.data_ptr() if need > 0 else 0, need, stream)
     if st != FA_OK:
         raise FAError(st)
     return out, lse

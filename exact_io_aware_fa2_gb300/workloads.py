@@ -68,6 +68,11 @@ WORKLOADS = {
         Workload("causal_b1_h16_n32768_d128_large_logits", 1, 16, 16, 32768,
                  32768, 128, True, q_std=3.0, k_spike_frac=0.01,
                  k_spike_mult=8.0),
+        # Few query rows over a long key sequence (a decode/prefill-chunk
+        # shape): 32 query blocks, so the split-KV schedule is what fills
+        # the GPU.  Not one of the pages' shapes; it measures that schedule.
+        Workload("splitkv_b1_hq32_hkv8_q128_kv32768_d128", 1, 32, 8, 128,
+                 32768, 128, False),
     ]
 }
 

@@ -23,11 +23,14 @@
  * GQA head sharing and the LSE output are this library's specification; the
  * pages do not define them.
  *
- * All functions are thread-safe and callable from any host thread.  The
- * library allocates no device memory.
+ * All functions are thread-safe and callable from any host thread.  Device
+ * memory: fa_fwd may take stream-ordered scratch from a per-device pool for
+ * the split-KV schedule (see fa_fwd_ws); nothing else is allocated.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
+
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -75,6 +78,41 @@ typedef enum {
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int Hq, int Hkv, int Nq, int Nkv, int D,
            float scale, int causal, void* stream);
+
+/*
+ * fa_fwd_ws — fa_fwd with caller-provided scratch memory.
+ *
+ * When the 256-row query blocks of a call fill fewer than half the SMs
+ * (decode-like or small-batch shapes), each block's key/value range is cut
+ * into contiguous pieces processed by separate CTAs ("split-KV", the
+ * FlashDecoding-style partition named on the "flash attention v3 paper"
+ * search page, second snippet).  Each piece leaves fp32 partial results
+ * (unnormalised O, running max, running sum per row) in scratch memory and
+ * a merge kernel combines them with the same rescaling the online softmax
+ * uses between key/value tiles.  fa_fwd takes that scratch from a
+ * per-device stream-ordered pool; fa_fwd_ws uses `workspace` instead.
+ *
+ *   workspace        device pointer, 16-byte aligned, at least
+ *                    fa_fwd_workspace_size() bytes; may be NULL when that
+ *                    size is 0.  Its contents on entry do not matter; the
+ *                    call overwrites it.  Calls that may run concurrently
+ *                    must not share it.
+ *   workspace_bytes  its size in bytes
+ * Other arguments, ownership and errors as fa_fwd; FA_ERR_INVALID_VALUE if
+ * the workspace is missing or too small, FA_ERR_MISALIGNED if unaligned.
+ */
+int fa_fwd_ws(const void* q, const void* k, const void* v, void* o,
+              float* lse, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+              float scale, int causal, void* workspace,
+              size_t workspace_bytes, void* stream);
+
+/*
+ * fa_fwd_workspace_size — bytes of scratch fa_fwd_ws needs for this shape on
+ * the current device; 0 when the shape is not split (then no scratch is
+ * used).  Writes *bytes and returns FA_OK; argument errors as fa_fwd.
+ */
+int fa_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                          int causal, size_t* bytes);
 
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* fa_status_string(int status);

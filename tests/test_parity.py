@@ -196,3 +196,66 @@ def test_bounded_wait_expires_into_status_and_context_survives():
     # the context is still usable
     w = WORKLOADS["tiny_128_d64"]
     full_compare(*make_inputs(w), w.scale, False, "after probe")
+
+
+# ------------------------------------------------ split-KV (few query blocks)
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("Nq,Nkv", [(1, 4096), (64, 3000), (200, 2500),
+                                    (300, 8192), (128, 640)])
+def test_split_kv_full(D, causal, Nq, Nkv):
+    """Shapes whose query blocks fill few SMs run split-KV (partials in
+    scratch plus a merge kernel); they must match the oracle everywhere."""
+    q, k, v = make_custom(1, 2, 1, Nq, Nkv, D, seed=Nq + 3 * Nkv)
+    print(full_compare(q, k, v, 1.0 / math.sqrt(D), causal,
+                       f"split D{D} c{causal} {Nq}x{Nkv}"))
+
+
+def test_split_kv_is_used_for_decode_shapes():
+    assert fa.workspace_size(1, 8, 8, 128, 32768, 128, False) > 0
+    assert fa.workspace_size(1, 2, 1, 1, 4096, 64, False) > 0
+    # causal query row 0 sees one key: nothing worth splitting
+    assert fa.workspace_size(1, 2, 1, 1, 4096, 64, True) == 0
+    w = WORKLOADS["pages_b1_h8_q4096_kv8192_d128"]
+    assert fa.workspace_size(w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D,
+                             w.causal) == 0
+
+
+def test_split_kv_large_logits_and_gqa():
+    q, k, v = make_custom(2, 8, 2, 150, 6000, 128, seed=21, q_std=3.0)
+    k[:, :, ::97] *= 8
+    print(full_compare(q, k, v, 0.0883883, True, "split large logits GQA"))
+
+
+def test_pool_scratch_and_caller_workspace_agree():
+    """fa_fwd (scratch from the library's pool) and fa_fwd_ws (caller's
+    workspace) run the same schedule and give identical bits."""
+    q, k, v = (t.cuda() for t in make_custom(1, 4, 2, 100, 5000, 128,
+                                             seed=15))
+    assert fa.workspace_size(1, 4, 2, 100, 5000, 128, False) > 0
+    o1, l1 = fa.fwd(q, k, v, scale=0.0883883, causal=False)
+    o2 = torch.empty_like(q)
+    l2 = torch.empty_like(l1)
+    st = fa.fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o2.data_ptr(),
+                    l2.data_ptr(), 1, 4, 2, 100, 5000, 128, 0.0883883, False,
+                    torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == 0 and fa.last_device_error() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_workspace_missing_or_small_is_rejected():
+    q, k, v = (t.cuda() for t in make_custom(1, 2, 2, 64, 3000, 64, seed=16))
+    need = fa.workspace_size(1, 2, 2, 64, 3000, 64, False)
+    assert need > 0
+    ws = torch.empty(need + 16, dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+    s = torch.cuda.current_stream().cuda_stream
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), 0,
+            1, 2, 2, 64, 3000, 64, 0.125, False)
+    assert fa.fwd_ws_raw(*args, ws.data_ptr(), need - 16, s) == 1
+    assert fa.fwd_ws_raw(*args, 0, 0, s) == 1
+    assert fa.fwd_ws_raw(*args, ws.data_ptr() + 4, need, s) == 3
+    assert fa.fwd_ws_raw(*args, ws.data_ptr(), need, s) == 0
+    torch.cuda.synchronize()
