@@ -333,6 +333,56 @@ int fa_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
   return FA_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Split-KV scratch for fa_fwd_noalloc: a fixed array in device memory, part
+// of the loaded module, so that entry point never allocates.  Each device
+// that loads the library holds it until the process exits.  In host code
+// the name only stands for the symbol; its device address comes from
+// cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char
+    g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+void* g_noalloc_ptr[kMaxDevices];
+
+// Device address of the array on the current device, looked up once per
+// device (with that device current).
+int noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  static std::once_flag flags[kMaxDevices];
+  static int status[kMaxDevices];
+  std::call_once(flags[dev], [dev] {
+    void* ptr = nullptr;
+    status[dev] = cudaGetSymbolAddress(&ptr, g_noalloc_scratch) == cudaSuccess
+                      ? FA_OK
+                      : FA_ERR_CUDA;
+    g_noalloc_ptr[dev] = ptr;
+  });
+  if (status[dev] == FA_OK) *out = g_noalloc_ptr[dev];
+  return status[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o,
+                   float* lse, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                   float scale, int causal, void* stream) {
+  size_t need = 0;
+  int st = fa_fwd_workspace_size(B, Hq, Hkv, Nq, Nkv, D, causal, &need);
+  if (st != FA_OK) return st;
+  if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_INVALID_VALUE;
+  void* scratch = nullptr;
+  if (need > 0 && (st = noalloc_scratch(&scratch)) != FA_OK) return st;
+  return fa_fwd_ws(q, k, v, o, lse, B, Hq, Hkv, Nq, Nkv, D, scale, causal,
+                   scratch, need, stream);
+}
+
 const char* fa_status_string(int status) {
   switch (status) {
     case FA_OK: return "FA_OK";

@@ -27,7 +27,7 @@ FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_VALUE", 2: "FA_ERR_UNSUPPORTED",
                 3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
 # Every symbol the header declares.
-SYMBOLS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size",
+SYMBOLS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_noalloc",
            "fa_status_string", "fa_last_device_error",
            "fa_probe_bounded_wait", "fa_version")
 
@@ -66,6 +66,9 @@ def load():
         lib.fa_fwd_workspace_size.argtypes = [
             ci, ci, ci, ci, ci, ci, ci, ctypes.POINTER(ctypes.c_size_t)]
         lib.fa_fwd_workspace_size.restype = ci
+        lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci,
+                                       ci, ctypes.c_float, ci, vp]
+        lib.fa_fwd_noalloc.restype = ci
         lib.fa_status_string.argtypes = [ci]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_last_device_error.argtypes = []
@@ -117,6 +120,21 @@ def fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, Nq, Nkv, D,
 
 
 _ws_cache = {}
+
+
+# Bytes of the fixed scratch array behind fa_fwd_noalloc.
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def fwd_noalloc_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, Nq, Nkv,
+                    D, scale, causal, stream_handle):
+    """Direct call of ``fa_fwd_noalloc`` (allocates nothing); returns the
+    status."""
+    return int(load().fa_fwd_noalloc(
+        ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+        ctypes.c_void_p(o_ptr), ctypes.c_void_p(lse_ptr),
+        B, Hq, Hkv, Nq, Nkv, D, ctypes.c_float(scale), 1 if causal else 0,
+        ctypes.c_void_p(stream_handle)))
 
 
 def workspace_size(B, Hq, Hkv, Nq, Nkv, D, causal):

@@ -114,6 +114,42 @@ int fa_fwd_ws(const void* q, const void* k, const void* v, void* o,
 int fa_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
                           int causal, size_t* bytes);
 
+/* Size of the fixed scratch array behind fa_fwd_noalloc (32 MiB). */
+#define FA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * fa_fwd_noalloc — fa_fwd for callers that must not allocate device memory.
+ *
+ * The pages describe no such call; it exists for callers that cannot call
+ * cudaMalloc or take memory from an allocator while they run: for example
+ * code that reserves all device memory up front and forbids allocation
+ * afterwards (a serving process with a fixed memory plan, a plugin inside a
+ * host framework that owns the allocator), or code on a latency-critical
+ * path where an allocation's cost or failure is not acceptable.
+ *
+ * It computes exactly what fa_fwd computes, with the same arguments, and
+ * allocates nothing: the split-KV scratch some shapes need (see fa_fwd_ws)
+ * lives in one fixed device array of FA_NOALLOC_SCRATCH_BYTES bytes that is
+ * part of the library and stays resident on every device that has loaded
+ * it until the process exits.  Shapes that need more scratch than that
+ * (fa_fwd_workspace_size() > FA_NOALLOC_SCRATCH_BYTES) are rejected with
+ * FA_ERR_INVALID_VALUE before anything is launched.  The scratch a shape
+ * needs grows with the GPU's SM count, not with the sequence lengths; on a
+ * 152-SM GB300 every supported shape needs at most about 30 MB, so none is
+ * rejected there.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any
+ * stream capture.  All calls on a device share the one array: two calls
+ * whose kernels may overlap on the GPU (different streams, no ordering
+ * between them) race on it and can corrupt each other's results.  Calls
+ * ordered on one stream are safe.  Each call overwrites every part of the
+ * array that it later reads, so nothing needs clearing between calls.
+ */
+int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o,
+                   float* lse, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                   float scale, int causal, void* stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* fa_status_string(int status);
 

@@ -105,3 +105,11 @@ def test_binding_rejects_bad_tensors():
         fa._check(qb, qb[:, :, :4], qb)
     with pytest.raises(ValueError):
         fa._check(qb.transpose(2, 3), qb, qb)
+
+
+def test_noalloc_limit_matches_header():
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+FA_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)",
+                  text)
+    assert m is not None
+    assert int(m.group(1)) << int(m.group(2)) == fa.NOALLOC_SCRATCH_BYTES
