@@ -123,26 +123,54 @@ int device_ready(int** word_out, int* dev_out = nullptr) {
 
 // Split-KV: when the pairs of query tiles fill fewer than half the SMs, cut
 // each pair's K/V range into contiguous pieces (at least kMinSplitBlocks
-// blocks each, at most kMaxSplits pieces) so about one CTA runs per SM.
+// blocks each, at most kMaxSplits pieces).  The count minimises the
+// estimated time: waves of CTAs x (blocks per piece + kSplitOverheadBlocks,
+// a piece's fixed cost for its Q load, set-up and fp32 partial write, in
+// units of one K/V block), the smaller count on a tie.
 constexpr int kMinSplitBlocks = 4;
 constexpr int kMaxSplits = 64;
+constexpr int kSplitOverheadBlocks = 3;
 
 int plan_splits(int B, int Hq, int Nq, int Nkv, int causal, int sms) {
   const long long pairs = (Nq + fa::kBM * fa::kTilesPerCta - 1) /
                           (fa::kBM * fa::kTilesPerCta);
   const long long ctas = pairs * Hq * B;
   if (ctas * 2 > sms) return 1;
-  int longest = (Nkv + fa::kBN - 1) / fa::kBN;           // K/V blocks
+  long long longest = (Nkv + fa::kBN - 1) / fa::kBN;     // K/V blocks
   if (causal) {
     const int rows = Nq < Nkv ? Nq : Nkv;
     longest = (rows + fa::kBN - 1) / fa::kBN;
   }
-  long long s = (sms + ctas - 1) / ctas;
-  const long long by_len = longest / kMinSplitBlocks;
-  if (s > by_len) s = by_len;
-  if (s > kMaxSplits) s = kMaxSplits;
-  if (s > 65535 / B) s = 65535 / B;                      // grid.z limit
-  return s < 1 ? 1 : static_cast<int>(s);
+  long long cap = longest / kMinSplitBlocks;
+  if (cap > kMaxSplits) cap = kMaxSplits;
+  if (cap > 65535 / B) cap = 65535 / B;                  // grid.z limit
+  long long best_s = 1, best_cost = -1;
+  for (long long s = 1; s <= cap; ++s) {
+    const long long waves = (ctas * s + sms - 1) / sms;
+    const long long cost =
+        waves * ((longest + s - 1) / s + kSplitOverheadBlocks);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_s = s;
+    }
+  }
+  return static_cast<int>(best_s);
+}
+
+// The shape the kernel runs.  Without a causal mask every query row of a
+// GQA group reads the same K/V, and the group's heads are adjacent in the
+// [B, Hq, Nq, D] layout (as are their O rows and LSE entries), so the group
+// runs as one head of (Hq / Hkv) * Nq rows: no padded query tile per head
+// and one pass over K/V per group.  With the mask a row's visible keys
+// depend on its index within its own head, so causal shapes run as given.
+struct RunShape {
+  int Hq, Nq;
+};
+
+RunShape run_shape(int Hq, int Hkv, int Nq, int causal) {
+  const long long packed = static_cast<long long>(Hq / Hkv) * Nq;
+  if (causal || Hq == Hkv || packed > (1ll << 30)) return {Hq, Nq};
+  return {Hkv, static_cast<int>(packed)};
 }
 
 int64_t workspace_bytes(int B, int Hq, int Nq, int D, int splits) {
@@ -249,6 +277,9 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
   int dev = 0;
   if ((st = device_ready(&word, &dev)) != FA_OK) return st;
 
+  const RunShape rs = run_shape(Hq, Hkv, Nq, causal);
+  Hq = rs.Hq;
+  Nq = rs.Nq;
   fa::FwdParams p;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
@@ -328,8 +359,10 @@ int fa_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
   int dev = 0;
   const int st = device_ready(nullptr, &dev);
   if (st != FA_OK) return st;
+  const RunShape rs = run_shape(Hq, Hkv, Nq, causal);
   *bytes = static_cast<size_t>(workspace_bytes(
-      B, Hq, Nq, D, plan_splits(B, Hq, Nq, Nkv, causal, g_sm_count[dev])));
+      B, rs.Hq, rs.Nq, D,
+      plan_splits(B, rs.Hq, rs.Nq, Nkv, causal, g_sm_count[dev])));
   return FA_OK;
 }
 

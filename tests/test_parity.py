@@ -228,6 +228,19 @@ def test_split_kv_large_logits_and_gqa():
     print(full_compare(q, k, v, 0.0883883, True, "split large logits GQA"))
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nkv,D", [
+    (1, 8, 1, 1, 2000, 128),       # one decode row per head, MQA
+    (3, 16, 2, 5, 3000, 128),      # batched GQA, few rows: packed and split
+    (2, 12, 4, 130, 700, 64),      # a packed query tile spans two heads
+])
+def test_gqa_heads_packed_non_causal(B, Hq, Hkv, Nq, Nkv, D):
+    """Non-causal GQA runs each group of query heads as one long head; O
+    and LSE must land in every head's own rows."""
+    q, k, v = make_custom(B, Hq, Hkv, Nq, Nkv, D, seed=Hq * Nq + Nkv)
+    print(full_compare(q, k, v, 1.0 / math.sqrt(D), False,
+                       f"packed GQA {B}x{Hq}/{Hkv} {Nq}x{Nkv} D{D}"))
+
+
 def test_pool_scratch_and_caller_workspace_agree():
     """fa_fwd (scratch from the library's pool) and fa_fwd_ws (caller's
     workspace) run the same schedule and give identical bits."""
