@@ -20,6 +20,10 @@ scaling).
 
 ``--impl reference`` times the CPU oracle (float64, host cores) on bounded
 samples of the same workload: one 128-row query tile per step.
+
+The line's ``sdpa`` object times torch's scaled_dot_product_attention
+(cuDNN, flash and memory-efficient backends, each alone) on the same inputs
+and in the same way, for comparison (``--no-sdpa`` skips it).
 """
 
 import argparse
@@ -56,6 +60,9 @@ def parse():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-sdpa", action="store_true",
+                    help="skip the torch SDPA comparison column")
+    ap.add_argument("--sdpa-steps", type=int, default=200)
     return ap.parse_args()
 
 
@@ -254,6 +261,66 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+SDPA_BACKENDS = ("CUDNN_ATTENTION", "FLASH_ATTENTION", "EFFICIENT_ATTENTION")
+
+
+def sdpa_column(w, q, k, v, o_ours, flush, stream, steps, warmup=5):
+    """torch's scaled_dot_product_attention on the same resident inputs, one
+    backend at a time, timed like our kernel (L2 flushed before each step,
+    CUDA events on the launching stream).  A comparison, not part of the
+    path.  Grouped-query shapes use SDPA's own GQA support; a backend that
+    lacks it gets K/V expanded to every query head beforehand (untimed),
+    which the entry notes.  Returns {backend: {...}} with TFLOPS and the
+    largest |O_sdpa - O_ours|, or the reason a backend did not run."""
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+    import torch.nn.functional as F
+    out = {}
+    for name in SDPA_BACKENDS:
+        backend = getattr(SDPBackend, name)
+        entry = {}
+        try:
+            kk, vv, gqa = k, v, w.Hq != w.Hkv
+            with sdpa_kernel([backend]):
+                def step():
+                    return F.scaled_dot_product_attention(
+                        q, kk, vv, is_causal=w.causal, scale=w.scale,
+                        enable_gqa=gqa)
+                try:
+                    res = step()
+                except RuntimeError:
+                    if not gqa:
+                        raise
+                    g = w.Hq // w.Hkv
+                    kk = k.repeat_interleave(g, dim=1)
+                    vv = v.repeat_interleave(g, dim=1)
+                    gqa = False
+                    entry["note"] = "K/V expanded to Hq heads (untimed)"
+                    res = step()
+                for _ in range(warmup):
+                    step()
+                torch.cuda.synchronize()
+                ev = [(torch.cuda.Event(enable_timing=True),
+                       torch.cuda.Event(enable_timing=True))
+                      for _ in range(steps)]
+                for i, (s, e) in enumerate(ev):
+                    flush.fill_(float(i))
+                    s.record(stream)
+                    step()
+                    e.record(stream)
+                torch.cuda.synchronize()
+            ms = sum(s.elapsed_time(e) for s, e in ev) / steps
+            entry.update({
+                "value": w.flops / (ms * 1e-3) / 1e12, "unit": UNIT,
+                "ms_per_step": ms, "steps": steps,
+                "max_abs_diff_vs_ours":
+                    float((res.float() - o_ours.float()).abs().max())})
+        except Exception as exc:  # a backend this GPU/torch cannot run
+            entry = {"unavailable": f"{type(exc).__name__}: "
+                                    f"{str(exc).splitlines()[0][:160]}"}
+        out[name.lower()] = entry
+    return out
+
+
 def run_ours(args, w):
     from exact_io_aware_fa2_gb300 import fa
     ws, rank, local = dist_env()
@@ -331,6 +398,10 @@ def run_ours(args, w):
     h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
 
+    sdpa = None
+    if ws == 1 and not args.no_sdpa:
+        sdpa = sdpa_column(w, q, k, v, o, flush, stream, args.sdpa_steps)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, q_h, k_h, v_h, args.cpu_seconds)
@@ -366,6 +437,7 @@ def run_ours(args, w):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s * 1e3},
         "gpu_launches": args.steps * launches_per_step,
+        "sdpa": sdpa,
         "clocks": clk.summary(),
         "wall_s_timed_loop": wall,
         "ms_per_step_min": min(per), "ms_per_step_median":
