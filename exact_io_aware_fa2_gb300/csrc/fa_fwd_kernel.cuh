@@ -120,12 +120,12 @@ struct FwdParams {
 template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dq,
                                          uint64_t dk, uint32_t idesc) {
-  mma_ss_c<0>(d_tmem, dq, dk, idesc);
+  mma_ss_w<0>(d_tmem, dq, dk, idesc);
 #pragma unroll
   for (int kk = 1; kk < D / 16; ++kk) {
     const uint64_t off = static_cast<uint64_t>(
         ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
-    mma_ss_c<1>(d_tmem, dq + off, dk + off, idesc);
+    mma_ss_w<1>(d_tmem, dq + off, dk + off, idesc);
   }
 }
 
@@ -137,11 +137,11 @@ template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t a_tmem,
                                          uint64_t dv, uint32_t idesc,
                                          bool acc) {
-  mma_ts(d_tmem, a_tmem, dv, idesc, acc ? 1u : 0u);
+  mma_ts_w(d_tmem, a_tmem, dv, idesc, acc ? 1u : 0u);
 #pragma unroll
   for (int kk = 1; kk < kBN / 16; ++kk)
-    mma_ts_c<1>(d_tmem, a_tmem + kk * 8,
-                dv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc);
+    mma_ts_wc<1>(d_tmem, a_tmem + kk * 8,
+                 dv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc);
 }
 
 // Number of K/V blocks a tile starting at query row `row0` visits.
@@ -282,50 +282,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ============================ MMA issuer ==============================
-    if (lane == 0) {
-      // Descriptors of every operand tile, built once.
-      const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
-      const uint64_t dK = sdesc_sw128(sK, 16, 1024);
-      const uint64_t dV = sdesc_sw128(sV, kBoxBytes, 1024);
-      constexpr uint64_t kStep = static_cast<uint64_t>(C::kTileBytes >> 4);
-      bool ok = mbar_wait(bQFull, 0, wc);
-      // j counts this CTA's blocks (ring position); block j0 + j of the pair
-      for (int j = 0; ok && j <= n_blocks; ++j) {
-        const int s = j % NK;                  // K stage of block j
-        const int sp = (j + NV - 1) % NV;      // V stage of block j-1
-        if (j >= 1 &&
-            !(ok = mbar_wait(bVFull(sp), ((j - 1) / NV) & 1, wc)))
-          break;
-        if (j < n_blocks && !(ok = mbar_wait(bKFull(s), (j / NK) & 1, wc)))
-          break;
-        const uint64_t dKs = dK + static_cast<uint64_t>(s) * kStep;
-        const uint64_t dVs = dV + static_cast<uint64_t>(sp) * kStep;
+    // The whole warp runs this loop, converged and with warp-uniform values;
+    // one elected lane issues each MMA and commit.  Wait outcomes are made
+    // warp-uniform before they steer control flow.
+    constexpr uint32_t kAll = 0xffffffffu;
+    // Descriptors of every operand tile, built once.
+    const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
+    const uint64_t dK = sdesc_sw128(sK, 16, 1024);
+    const uint64_t dV = sdesc_sw128(sV, kBoxBytes, 1024);
+    constexpr uint64_t kStep = static_cast<uint64_t>(C::kTileBytes >> 4);
+    bool ok = __all_sync(kAll, mbar_wait(bQFull, 0, wc));
+    // j counts this CTA's blocks (ring position); block j0 + j of the pair
+    for (int j = 0; ok && j <= n_blocks; ++j) {
+      const int s = j % NK;                  // K stage of block j
+      const int sp = (j + NV - 1) % NV;      // V stage of block j-1
+      if (j >= 1 &&
+          !(ok = __all_sync(kAll, mbar_wait(bVFull(sp), ((j - 1) / NV) & 1,
+                                            wc))))
+        break;
+      if (j < n_blocks &&
+          !(ok = __all_sync(kAll, mbar_wait(bKFull(s), (j / NK) & 1, wc))))
+        break;
+      const uint64_t dKs = dK + static_cast<uint64_t>(s) * kStep;
+      const uint64_t dVs = dV + static_cast<uint64_t>(sp) * kStep;
 #pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          // O_x += P_x(j-1) V_{j-1}
-          if (j >= 1 && j0 + j - 1 < nblk[x]) {
-            if (!(ok = mbar_wait(bPFull(x), (j - 1) & 1, wc))) break;
-            tc_fence_after();
-            issue_pv<D>(tmem + C::col_o(x), tmem + C::col_p(x), dVs,
-                        C::kIdescPV, j > 1);
-          }
-          // S_x(j) = Q_x K_j^T
-          if (j < n_blocks && j0 + j < nblk[x]) {
-            issue_qk<D>(tmem + C::col_s(x),
-                        dQ + static_cast<uint64_t>(x) * kStep, dKs,
-                        C::kIdescS);
-            mma_commit(bSFull(x));
-          }
+      for (int x = 0; x < 2; ++x) {
+        // O_x += P_x(j-1) V_{j-1}
+        if (j >= 1 && j0 + j - 1 < nblk[x]) {
+          if (!(ok = __all_sync(kAll,
+                                mbar_wait(bPFull(x), (j - 1) & 1, wc))))
+            break;
+          tc_fence_after();
+          issue_pv<D>(tmem + C::col_o(x), tmem + C::col_p(x), dVs,
+                      C::kIdescPV, j > 1);
         }
-        if (!ok) break;
-        if (j < n_blocks) mma_commit(bKEmpty(s));
-        if (j >= 1) mma_commit(bVEmpty(sp));
+        // S_x(j) = Q_x K_j^T
+        if (j < n_blocks && j0 + j < nblk[x]) {
+          issue_qk<D>(tmem + C::col_s(x),
+                      dQ + static_cast<uint64_t>(x) * kStep, dKs,
+                      C::kIdescS);
+          mma_commit_w(bSFull(x));
+        }
       }
-      mma_commit(bOFinal);
-      // Every MMA this thread issued completes before the CTA tears down.
-      mma_commit(bDrain);
-      mbar_wait(bDrain, 0, wc, false);
+      if (!ok) break;
+      if (j < n_blocks) mma_commit_w(bKEmpty(s));
+      if (j >= 1) mma_commit_w(bVEmpty(sp));
     }
+    mma_commit_w(bOFinal);
+    // Every MMA this warp issued completes before the CTA tears down.
+    mma_commit_w(bDrain);
+    mbar_wait(bDrain, 0, wc, false);
   } else {
     // ============================ softmax warps ===========================
     const int x = (warp - kSoftmaxWarp0) >> 2;     // tile A (0) or B (1)

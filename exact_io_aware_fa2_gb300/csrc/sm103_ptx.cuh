@@ -182,63 +182,57 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn,
          ((static_cast<uint32_t>(M) >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc,
-                                       uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
-          d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem], issued by one thread.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem,
-                                       uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
-          d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Same, with the accumulate flag a compile-time constant (no runtime setp
-// operand), for the unrolled issue loops.
+// Warp-wide forms: every lane of a converged warp executes the call with the
+// same operands and one lane, chosen by elect.sync, issues the instruction.
+// Keeping the issuing code warp-uniform lets the compiler hold descriptors
+// and TMEM addresses in uniform registers, which makes each issue cheap.
+//   mma_ss_w:  D[tmem] (+)= A[smem] * B[smem]^T
+//   mma_ts_w:  D[tmem] (+)= A[tmem] * B[smem]   (accumulate flag at run time)
+//   mma_ts_wc: the same with the flag a compile-time constant
 template <int ACC>
-__device__ __forceinline__ void mma_ss_c(uint32_t d_tmem, uint64_t a_desc,
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc,
                                          uint64_t b_desc, uint32_t idesc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
           d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(ACC)
       : "memory");
 }
-template <int ACC>
-__device__ __forceinline__ void mma_ts_c(uint32_t d_tmem, uint32_t a_tmem,
-                                         uint64_t b_desc, uint32_t idesc) {
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem,
+                                         uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+template <int ACC>
+__device__ __forceinline__ void mma_ts_wc(uint32_t d_tmem, uint32_t a_tmem,
+                                          uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
           d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "n"(ACC)
       : "memory");
 }
-
 // Arrive once on `bar` when every tcgen05 operation issued so far by this
-// thread has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
+// warp has completed.
+__device__ __forceinline__ void mma_commit_w(uint32_t bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
-      "[%0];" ::"r"(bar)
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
+      "[%0];\n\t}" ::"r"(bar)
       : "memory");
 }
 
