@@ -236,13 +236,15 @@ bool aligned(const void* p, uintptr_t a) {
 
 __global__ void probe_wait_kernel(int* status, uint64_t limit_ns) {
   __shared__ __align__(8) uint64_t bar_mem;
-  __shared__ uint32_t abort_flag;
+  __shared__ fa::WaitState ws;
   if (threadIdx.x == 0) {
     fa::mbar_init(fa::smem_addr(&bar_mem), 1);
-    abort_flag = 0;
+    ws.abort = 0;
+    ws.status = status;
+    ws.limit_ns = limit_ns;
     fa::mbar_init_fence();
     // Nothing arrives on this barrier: the wait must run out.
-    const fa::WaitCtx wc{&abort_flag, status, limit_ns};
+    const fa::WaitCtx wc{fa::smem_addr(&ws)};
     fa::mbar_wait(fa::smem_addr(&bar_mem), 0, wc);
   }
   __syncwarp();

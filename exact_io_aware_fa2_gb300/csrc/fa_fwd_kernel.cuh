@@ -76,7 +76,8 @@ struct FwdCfg {
   // barriers: Q, K full/empty, V full/empty, S full x2, P full x2, O final,
   // drain
   static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1 + 1;
-  static constexpr int kBarBytes = 8 * kNumBars + 16;  // + tmem slot + abort
+  // + tmem slot (8 bytes with padding) + the wait state (24 bytes)
+  static constexpr int kBarBytes = 8 * kNumBars + 32;
   static constexpr int kSmemBytes =
       1024 /*alignment slack*/ +
       kTileBytes * (kTilesPerCta + kKStages + kVStages) + kBarBytes;
@@ -209,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bDrain = bar(kB0 + 5);
   uint8_t* const misc = base_ptr + (sBar - base) + 8 * C::kNumBars;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
-  volatile uint32_t* const abort = reinterpret_cast<uint32_t*>(misc + 4);
+  WaitState* const wstate = reinterpret_cast<WaitState*>(misc + 8);
 
   if (threadIdx.x == 0) {
     mbar_init(bQFull, 1);
@@ -227,7 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bOFinal, 1);
     mbar_init(bDrain, 1);
-    *abort = 0u;
+    wstate->abort = 0u;
+    wstate->status = p.status;
+    wstate->limit_ns = p.wait_limit_ns;
     mbar_init_fence();
   }
   if (warp == kMmaWarp) {
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const WaitCtx wc{abort, p.status, p.wait_limit_ns};
+  const WaitCtx wc{smem_addr(wstate)};
 
   if (warp == kLoadWarp) {
     // ============================ TMA producer ============================

@@ -8,6 +8,7 @@
 // error code instead of a hang.
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -16,13 +17,23 @@ namespace fa {
 
 constexpr int kStatusTimeout = 5;  // == FA_ERR_TIMEOUT
 
-// What a bounded wait needs: the CTA's shared abort flag (raised by the first
-// role that gives up, so the others stop waiting too), the device status word
-// the host reads back, and the wall-clock limit of one wait.
-struct WaitCtx {
-  volatile uint32_t* abort;
+// What a bounded wait needs, kept in the CTA's shared memory: the abort flag
+// (raised by the first role that gives up, so the others stop waiting too),
+// the device status word the host reads back, and the wall-clock limit of one
+// wait.  Waiting threads carry only its shared-memory address, which keeps
+// the state out of their registers.
+struct WaitState {
+  uint32_t abort;
+  uint32_t pad;
   int* status;
   uint64_t limit_ns;
+};
+// mbar_wait reads the fields at these byte offsets.
+static_assert(offsetof(WaitState, status) == 8 &&
+                  offsetof(WaitState, limit_ns) == 16,
+              "WaitState layout");
+struct WaitCtx {
+  uint32_t state;  // shared::cta address of a WaitState
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -77,6 +88,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // limit; on expiry it records the timeout status, raises the abort flag and
 // returns false.  With `honour_abort` false it ignores the flag (used to
 // drain copies that are already in flight) but still stops at the limit.
+__device__ __forceinline__ uint32_t wait_aborted(const WaitCtx& w) {
+  uint32_t v;
+  asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(w.state));
+  return v;
+}
+__device__ __forceinline__ void wait_raise_abort(const WaitCtx& w) {
+  asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(w.state), "r"(1u)
+               : "memory");
+}
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           const WaitCtx& w,
                                           bool honour_abort = true) {
@@ -84,10 +105,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (honour_abort && *w.abort) return false;
-    if (globaltimer_ns() - t0 > w.limit_ns) {
-      atomicCAS(w.status, 0, kStatusTimeout);
-      *w.abort = 1u;
+    if (honour_abort && wait_aborted(w)) return false;
+    uint64_t limit;
+    asm volatile("ld.shared.u64 %0, [%1 + 16];" : "=l"(limit) : "r"(w.state));
+    if (globaltimer_ns() - t0 > limit) {
+      uint64_t status;
+      asm volatile("ld.shared.u64 %0, [%1 + 8];" : "=l"(status) : "r"(w.state));
+      atomicCAS(reinterpret_cast<int*>(status), 0, kStatusTimeout);
+      wait_raise_abort(w);
       return false;
     }
   }
