@@ -12,6 +12,7 @@
 
 #include "fa.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_fwd_wide.cuh"
 
 namespace fa {
 // Device-side status word (one per device), written by bounded waits that
@@ -59,6 +60,20 @@ cudaError_t opt_in_smem() {
                               fa::FwdCfg<D>::kSmemBytes);
 }
 
+template <int D, bool CAUSAL>
+cudaError_t opt_in_smem_wide() {
+  return cudaFuncSetAttribute(fa::fa_fwd_wide_kernel<D, CAUSAL>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              fa::WideCfg<D>::kSmemBytes);
+}
+
+// Head dims with a kernel: 64 and 128 (two query tiles per CTA, split-KV
+// capable) and 192 and 256 (one query tile per CTA, fa_fwd_wide.cuh).
+bool supported_head_dim(int D) {
+  return D == 64 || D == 128 || D == 192 || D == 256;
+}
+bool wide_head_dim(int D) { return D == 192 || D == 256; }
+
 int* g_status_word[kMaxDevices];
 int g_sm_count[kMaxDevices];
 cudaMemPool_t g_pool[kMaxDevices];
@@ -89,7 +104,11 @@ int device_ready(int** word_out, int* dev_out = nullptr) {
     if (opt_in_smem<64, false>() != cudaSuccess ||
         opt_in_smem<64, true>() != cudaSuccess ||
         opt_in_smem<128, false>() != cudaSuccess ||
-        opt_in_smem<128, true>() != cudaSuccess) {
+        opt_in_smem<128, true>() != cudaSuccess ||
+        opt_in_smem_wide<192, false>() != cudaSuccess ||
+        opt_in_smem_wide<192, true>() != cudaSuccess ||
+        opt_in_smem_wide<256, false>() != cudaSuccess ||
+        opt_in_smem_wide<256, true>() != cudaSuccess) {
       status[dev] = FA_ERR_CUDA;
       return;
     }
@@ -182,11 +201,11 @@ int64_t workspace_bytes(int B, int Hq, int Nq, int D, int splits) {
   return static_cast<int64_t>(B) * Hq * pairs * splits * slot * 4;
 }
 
-// Tensor map of a contiguous bf16 [BH, N, D] tensor, read in 64 x 128 boxes
-// (64 head-dim elements = one 128-byte swizzle row, 128 sequence rows) with
-// the 128-byte swizzle.  Rows past N are zero-filled by the TMA unit.
+// Tensor map of a contiguous bf16 [BH, N, D] tensor, read in boxes of 64
+// head-dim elements (one 128-byte swizzle row) by `box_rows` sequence rows,
+// with the 128-byte swizzle.  Rows past N are zero-filled by the TMA unit.
 int encode_bhnd(CUtensorMap* map, const void* ptr, long long BH, int N,
-                int D) {
+                int D, int box_rows = fa::kBM) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return FA_ERR_CUDA;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D),
@@ -195,7 +214,7 @@ int encode_bhnd(CUtensorMap* map, const void* ptr, long long BH, int N,
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                            static_cast<cuuint64_t>(N) * D * 2};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(fa::kBoxCols),
-                       static_cast<cuuint32_t>(fa::kBM), 1};
+                       static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t elem_strides[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                    const_cast<void*>(ptr), dims, strides, box, elem_strides,
@@ -230,6 +249,17 @@ int launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
   return FA_OK;
 }
 
+template <int D, bool CAUSAL>
+int launch_wide(const CUtensorMap& q, const CUtensorMap& k,
+                const CUtensorMap& v, const fa::FwdParams& p, int B, int Hq,
+                int Nq, cudaStream_t stream) {
+  dim3 grid((Nq + fa::kBM - 1) / fa::kBM, Hq, B);
+  fa::fa_fwd_wide_kernel<D, CAUSAL>
+      <<<grid, fa::kWideThreads, fa::WideCfg<D>::kSmemBytes, stream>>>(q, k, v,
+                                                                       p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }
@@ -260,7 +290,7 @@ int check_args(const void* q, const void* k, const void* v, const void* o,
   if (Hq % Hkv != 0) return FA_ERR_INVALID_VALUE;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_VALUE;
   if (B > 65535 || Hq > 65535) return FA_ERR_INVALID_VALUE;  // grid limits
-  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (!supported_head_dim(D)) return FA_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
       !aligned(o, 16) || (lse != nullptr && !aligned(lse, 4)))
     return FA_ERR_MISALIGNED;
@@ -293,7 +323,10 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
                                     1.4426950408889634074);
   p.status = word;
   p.wait_limit_ns = kWaitLimitNs;
-  p.kv_splits = plan_splits(B, Hq, Nq, Nkv, causal, g_sm_count[dev]);
+  // The wide-head kernel has no split-KV form.
+  p.kv_splits = wide_head_dim(D)
+                    ? 1
+                    : plan_splits(B, Hq, Nq, Nkv, causal, g_sm_count[dev]);
   p.work = nullptr;
   const int64_t need = workspace_bytes(B, Hq, Nq, D, p.kv_splits);
   void* owned = nullptr;
@@ -312,13 +345,22 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
   }
 
   CUtensorMap tq, tk, tv;
+  const int kv_rows = wide_head_dim(D) ? fa::kWideBN : fa::kBN;
   if ((st = encode_bhnd(&tq, q, static_cast<long long>(B) * Hq, Nq, D)) ||
-      (st = encode_bhnd(&tk, k, static_cast<long long>(B) * Hkv, Nkv, D)) ||
-      (st = encode_bhnd(&tv, v, static_cast<long long>(B) * Hkv, Nkv, D))) {
+      (st = encode_bhnd(&tk, k, static_cast<long long>(B) * Hkv, Nkv, D,
+                        kv_rows)) ||
+      (st = encode_bhnd(&tv, v, static_cast<long long>(B) * Hkv, Nkv, D,
+                        kv_rows))) {
     if (owned != nullptr) cudaFreeAsync(owned, s);
     return st;
   }
-  if (D == 64)
+  if (D == 256)
+    st = causal ? launch_wide<256, true>(tq, tk, tv, p, B, Hq, Nq, s)
+                : launch_wide<256, false>(tq, tk, tv, p, B, Hq, Nq, s);
+  else if (D == 192)
+    st = causal ? launch_wide<192, true>(tq, tk, tv, p, B, Hq, Nq, s)
+                : launch_wide<192, false>(tq, tk, tv, p, B, Hq, Nq, s);
+  else if (D == 64)
     st = causal ? launch<64, true>(tq, tk, tv, p, B, Hq, Nq, s)
                 : launch<64, false>(tq, tk, tv, p, B, Hq, Nq, s);
   else
@@ -357,14 +399,16 @@ int fa_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
   if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nkv < 1 || D < 1 ||
       Hq % Hkv != 0 || B > 65535 || Hq > 65535)
     return FA_ERR_INVALID_VALUE;
-  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (!supported_head_dim(D)) return FA_ERR_UNSUPPORTED;
   int dev = 0;
   const int st = device_ready(nullptr, &dev);
   if (st != FA_OK) return st;
   const RunShape rs = run_shape(Hq, Hkv, Nq, causal);
   *bytes = static_cast<size_t>(workspace_bytes(
       B, rs.Hq, rs.Nq, D,
-      plan_splits(B, rs.Hq, rs.Nq, Nkv, causal, g_sm_count[dev])));
+      wide_head_dim(D)
+          ? 1
+          : plan_splits(B, rs.Hq, rs.Nq, Nkv, causal, g_sm_count[dev])));
   return FA_OK;
 }
 

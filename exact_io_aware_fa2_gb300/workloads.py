@@ -73,6 +73,14 @@ WORKLOADS = {
         # the GPU.  Not one of the pages' shapes; it measures that schedule.
         Workload("splitkv_b1_hq32_hkv8_q128_kv32768_d128", 1, 32, 8, 128,
                  32768, 128, False),
+        # The pages' shape with wide heads (head_dim 192 and 256), run by
+        # the one-tile-per-CTA kernel.
+        Workload("wide_b1_h8_q4096_kv8192_d192", 1, 8, 8, 4096, 8192, 192,
+                 False),
+        Workload("wide_b1_h8_q4096_kv8192_d256", 1, 8, 8, 4096, 8192, 256,
+                 False),
+        Workload("wide_causal_b1_h8_n8192_d256", 1, 8, 8, 8192, 8192, 256,
+                 True),
     ]
 }
 

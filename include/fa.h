@@ -41,7 +41,8 @@ typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID_VALUE = 1, /* null pointer, dimension < 1, Hq % Hkv != 0,
                                  non-finite scale, size beyond the limits   */
-    FA_ERR_UNSUPPORTED = 2,   /* D not in {64, 128}, or the current device is
+    FA_ERR_UNSUPPORTED = 2,   /* D not in {64, 128, 192, 256}, or the
+                                 current device is
                                  not compute capability 10.3 (sm_103)       */
     FA_ERR_MISALIGNED = 3,    /* q, k, v or o not 16-byte aligned, or lse not
                                  4-byte aligned (TMA needs 16 bytes)        */
@@ -60,7 +61,8 @@ typedef enum {
  *   o    device pointer, bf16 [B, Hq,  Nq,  D], contiguous; written
  *   lse  device pointer, fp32 [B, Hq,  Nq], contiguous; written; may be NULL
  *   B, Hq, Hkv, Nq, Nkv, D   sizes; Hq must be a multiple of Hkv (query head
- *        h reads kv head h / (Hq / Hkv)); D in {64, 128}
+ *        h reads kv head h / (Hq / Hkv)); D in {64, 128, 192, 256}
+ *        (192 and 256 run a one-query-tile-per-CTA kernel without split-KV)
  *   scale  finite fp32 multiplier of Q K^T (typically 1/sqrt(D))
  *   causal 0: every key visible; nonzero: key j visible to query i iff j <= i
  *   stream a cudaStream_t (as void*); NULL means the legacy default stream

@@ -73,7 +73,7 @@ def test_invalid_values_rejected_before_launch(lib, kw):
     assert _call(**kw) == 1  # FA_ERR_INVALID_VALUE
 
 
-@pytest.mark.parametrize("D", [1, 16, 32, 80, 96, 192, 256])
+@pytest.mark.parametrize("D", [1, 16, 32, 80, 96, 160, 224, 320, 512])
 def test_unsupported_head_dims(lib, D):
     assert _call(D=D) == 2  # FA_ERR_UNSUPPORTED
 

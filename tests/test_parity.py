@@ -171,9 +171,11 @@ def test_workload_full_size_sampled(name):
 
 
 @pytest.mark.parametrize("name", ["pages_b1_h8_q4096_kv8192_d128",
-                                  "causal_b4_h16_n2048_d64"])
+                                  "causal_b4_h16_n2048_d64",
+                                  "wide_b1_h8_q4096_kv8192_d256"])
 def test_workload_full_compare_some_heads(name):
-    """Whole heads of the headline and D=64 workloads, element by element."""
+    """Whole heads of the headline, D=64 and D=256 workloads, element by
+    element."""
     w = WORKLOADS[name]
     q, k, v = make_inputs(w)
     o, lse = run_gpu(q, k, v, w.scale, w.causal)
@@ -239,6 +241,35 @@ def test_gqa_heads_packed_non_causal(B, Hq, Hkv, Nq, Nkv, D):
     q, k, v = make_custom(B, Hq, Hkv, Nq, Nkv, D, seed=Hq * Nq + Nkv)
     print(full_compare(q, k, v, 1.0 / math.sqrt(D), False,
                        f"packed GQA {B}x{Hq}/{Hkv} {Nq}x{Nkv} D{D}"))
+
+
+# ------------------------------------------------------------ wide heads
+
+@pytest.mark.parametrize("D", [192, 256])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nkv", [(128, 128), (64, 64), (300, 200),
+                                    (200, 300), (1, 513), (640, 640)])
+def test_wide_heads_full(D, causal, Nq, Nkv):
+    """Head dims 192 and 256 run the one-tile kernel with 64-key blocks and
+    two score buffers; ragged tails of both sequences included."""
+    q, k, v = make_custom(1, 2, 1, Nq, Nkv, D, seed=D + Nq * 3 + Nkv)
+    print(full_compare(q, k, v, 1.0 / math.sqrt(D), causal,
+                       f"wide D{D} c{causal} {Nq}x{Nkv}"))
+
+
+@pytest.mark.parametrize("D", [192, 256])
+def test_wide_heads_gqa_batched_large_logits(D):
+    q, k, v = make_custom(2, 6, 2, 333, 1100, D, seed=D, q_std=3.0)
+    k[:, :, ::53] *= 8
+    print(full_compare(q, k, v, 1.0 / math.sqrt(D), True,
+                       f"wide D{D} GQA large logits causal"))
+    print(full_compare(q, k, v, 1.0 / math.sqrt(D), False,
+                       f"wide D{D} GQA large logits"))
+
+
+def test_wide_heads_need_no_workspace():
+    assert fa.workspace_size(1, 8, 8, 128, 32768, 256, False) == 0
+    assert fa.workspace_size(1, 8, 2, 1, 4096, 192, False) == 0
 
 
 def test_pool_scratch_and_caller_workspace_agree():
