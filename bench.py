@@ -27,7 +27,6 @@ and in the same way, for comparison (``--no-sdpa`` skips it).
 """
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -101,28 +100,41 @@ def peaks():
     return FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16"
 
 
-def kernel_source_hash():
-    """Hash of the device code (the kernel headers); host-side changes in
-    the API file leave recorded counters valid."""
+# Device-code headers of each attention kernel (host-side changes in the API
+# file leave recorded counters valid).
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": ("fa_fwd_kernel.cuh", "sm103_ptx.cuh"),
+    "fa_fwd_wide_kernel": ("fa_fwd_wide.cuh", "fa_fwd_kernel.cuh",
+                           "sm103_ptx.cuh"),
+}
+
+
+def kernel_for(w):
+    """The kernel that runs a workload (head dims 192 and 256 take the
+    one-tile kernel)."""
+    return "fa_fwd_wide_kernel" if w.D in (192, 256) else "fa_fwd_kernel"
+
+
+def kernel_source_hash(kernel="fa_fwd_kernel"):
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(
-            ROOT, "exact_io_aware_fa2_gb300", "csrc", "*.cuh"))):
+    for name in sorted(KERNEL_SOURCES[kernel]):
+        p = os.path.join(ROOT, "exact_io_aware_fa2_gb300", "csrc", name)
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload):
+def recorded_traffic(w):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+    on the current sources of the workload's kernel; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    e = d.get(workload)
-    if not e or e.get("kernel_src_sha") != kernel_source_hash():
+    e = d.get(w.name)
+    if not e or e.get("kernel_src_sha") != kernel_source_hash(kernel_for(w)):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -428,9 +440,9 @@ def run_ours(args, w):
                      "frac": per_launch_tflops / peak,
                      "peak_source": peak_src + ", of measured"
                      if "MEASURED" in peak_src else peak_src + ", of fallback",
-                     "traffic": recorded_traffic(w.name),
+                     "traffic": recorded_traffic(w),
                      "kernel": "fa_fwd_kernel<SPLIT> + fa_merge_kernel"
-                     if split else "fa_fwd_kernel",
+                     if split else kernel_for(w),
                      "algorithmic_flops_per_launch": w.flops},
         "cpu_baseline": cpu,
         "e2e": {"value": job_tflops(w.flops, e2e_s * 1e3, ws), "unit": UNIT,

@@ -345,7 +345,9 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
   }
 
   CUtensorMap tq, tk, tv;
-  const int kv_rows = wide_head_dim(D) ? fa::kWideBN : fa::kBN;
+  const int kv_rows = !wide_head_dim(D) ? fa::kBN
+                      : D == 192          ? fa::WideCfg<192>::kBN
+                                          : fa::WideCfg<256>::kBN;
   if ((st = encode_bhnd(&tq, q, static_cast<long long>(B) * Hq, Nq, D)) ||
       (st = encode_bhnd(&tk, k, static_cast<long long>(B) * Hkv, Nkv, D,
                         kv_rows)) ||

@@ -35,7 +35,6 @@
 
 namespace fa {
 
-constexpr int kWideBN = 64;            // keys per K/V block
 constexpr int kWideThreads = 192;
 constexpr int kWideMmaWarp = 0;
 constexpr int kWideLoadWarp = 1;
@@ -44,9 +43,11 @@ constexpr int kWideSoftmaxWarp0 = 2;
 template <int D>
 struct WideCfg {
   static_assert(D == 192 || D == 256, "wide head dim");
+  // keys per K/V block: TMEM holds two S buffers of kBN columns and O
+  static constexpr int kBN = 64;
   static constexpr int kBoxes = D / kBoxCols;              // 64-column boxes
   static constexpr int kQBoxBytes = kBM * kBoxCols * 2;    // 128 rows: 16 KiB
-  static constexpr int kKVBoxBytes = kWideBN * kBoxCols * 2;  // 64 rows: 8 KiB
+  static constexpr int kKVBoxBytes = kBN * kBoxCols * 2;   // kBN rows
   static constexpr int kQBytes = kBoxes * kQBoxBytes;
   static constexpr int kKVBytes = kBoxes * kKVBoxBytes;
   // K_{j+1} is needed one step before V_j (S(j+1) is issued before PV(j)),
@@ -60,15 +61,15 @@ struct WideCfg {
   static constexpr int kSmemBytes = 1024 + kQBytes +
                                     (kKStages + kVStages) * kKVBytes +
                                     kBarBytes;
-  static constexpr uint32_t kColO = 2 * kWideBN;
-  static constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kWideBN, false, false);
+  static constexpr uint32_t kColO = 2 * kBN;
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);
 };
 
-// S = Q K^T for one 64-key block: D/16 MMAs of 128x64x16, both operands
+// S = Q K^T for one block: D/16 MMAs of 128 x kBN x 16, both operands
 // K-major with the 128-byte swizzle.  Stepping K by 16 elements moves 32
 // bytes within a swizzle row and, every 64 elements, to the next box (16 KiB
-// for the 128-row Q box, 8 KiB for the 64-row K box).
+// for the 128-row Q box, kBN * 128 bytes for the K box).
 template <int D>
 __device__ __forceinline__ void wide_issue_qk(uint32_t d_tmem, uint64_t dq,
                                               uint64_t dk, uint32_t idesc) {
@@ -85,15 +86,16 @@ __device__ __forceinline__ void wide_issue_qk(uint32_t d_tmem, uint64_t dq,
   }
 }
 
-// O += P V for one 64-key block: 4 MMAs of 128xDx16.  P (bf16x2, 8 TMEM
+// O += P V for one block: kBN/16 MMAs of 128xDx16.  P (bf16x2, 8 TMEM
 // columns per 16 keys) comes from TMEM; V is MN-major with the 128-byte
 // swizzle (16 keys = 2048 bytes).
+template <int D>
 __device__ __forceinline__ void wide_issue_pv(uint32_t d_tmem, uint32_t a_tmem,
                                               uint64_t dv, uint32_t idesc,
                                               bool acc) {
   mma_ts_w(d_tmem, a_tmem, dv, idesc, acc ? 1u : 0u);
 #pragma unroll
-  for (int kk = 1; kk < kWideBN / 16; ++kk)
+  for (int kk = 1; kk < WideCfg<D>::kBN / 16; ++kk)
     mma_ts_wc<1>(d_tmem, a_tmem + kk * 8,
                  dv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc);
 }
@@ -105,6 +107,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                        const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ FwdParams p) {
   using W = WideCfg<D>;
+  constexpr int BN = W::kBN;
   constexpr int NK = W::kKStages;
   constexpr int NV = W::kVStages;
   constexpr uint32_t kAll = 0xffffffffu;
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const int hk = hq / (p.Hq / p.Hkv);
   const int row0 = tile * kBM;
   const int kv_end = CAUSAL ? min(p.Nkv, row0 + kBM) : p.Nkv;
-  const int nblk = (kv_end + kWideBN - 1) / kWideBN;
+  const int nblk = (kv_end + BN - 1) / BN;
 
   // ---- shared memory (1024-byte aligned for the swizzle atoms) ----
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -199,13 +202,13 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         mbar_arrive_expect_tx(bKFull(sk), W::kKVBytes);
         for (int c = 0; c < W::kBoxes; ++c)
           tma_load_3d(sK + sk * W::kKVBytes + c * W::kKVBoxBytes, &tmK,
-                      bKFull(sk), c * kBoxCols, j * kWideBN, zk, keep);
+                      bKFull(sk), c * kBoxCols, j * BN, zk, keep);
         k_issued = j + 1;
         if (!mbar_wait(bVEmpty(sv), ((j / NV) & 1) ^ 1, wc)) break;
         mbar_arrive_expect_tx(bVFull(sv), W::kKVBytes);
         for (int c = 0; c < W::kBoxes; ++c)
           tma_load_3d(sV + sv * W::kKVBytes + c * W::kKVBoxBytes, &tmV,
-                      bVFull(sv), c * kBoxCols, j * kWideBN, zk, keep);
+                      bVFull(sv), c * kBoxCols, j * BN, zk, keep);
         v_issued = j + 1;
       }
       // Never leave the CTA with copies in flight.
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         const int s = jn % NK;
         if (!(ok = __all_sync(kAll, mbar_wait(bKFull(s), (jn / NK) & 1, wc))))
           break;
-        wide_issue_qk<D>(tmem + static_cast<uint32_t>((jn & 1) * kWideBN), dQ,
+        wide_issue_qk<D>(tmem + static_cast<uint32_t>((jn & 1) * BN), dQ,
                          dK + static_cast<uint64_t>(s) * kKVStep, W::kIdescS);
         mma_commit_w(bSFull(jn & 1));
         mma_commit_w(bKEmpty(s));
@@ -242,8 +245,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                               mbar_wait(bPFull(j & 1), (j >> 1) & 1, wc))))
           break;
         tc_fence_after();
-        wide_issue_pv(tmem + W::kColO,
-                      tmem + static_cast<uint32_t>((j & 1) * kWideBN),
+        wide_issue_pv<D>(tmem + W::kColO,
+                      tmem + static_cast<uint32_t>((j & 1) * BN),
                       dV + static_cast<uint64_t>(sv) * kKVStep, W::kIdescPV,
                       j > 0);
         mma_commit_w(bPVDone);
@@ -267,49 +270,52 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       if (!(ok = __all_sync(kAll, mbar_wait(bSFull(u), (j >> 1) & 1, wc))))
         break;
       tc_fence_after();
-      uint32_t sr[kWideBN];
+      uint32_t sr[BN];
       const uint32_t s_addr =
-          tmem + lane_off + static_cast<uint32_t>(u * kWideBN);
-      const int col0 = j * kWideBN;
+          tmem + lane_off + static_cast<uint32_t>(u * BN);
+      const int col0 = j * BN;
       const bool need_mask =
-          (col0 + kWideBN > p.Nkv) || (CAUSAL && col0 + kWideBN - 1 > row0);
-      float red[kWideBN / 32];
+          (col0 + BN > p.Nkv) || (CAUSAL && col0 + BN - 1 > row0);
+      float red[BN / 32];
       if (!need_mask && !neg_scale) {
 #pragma unroll
-        for (int cc = 0; cc < kWideBN / 32; ++cc)
+        for (int cc = 0; cc < BN / 32; ++cc)
           tmem_ld32_max(s_addr + cc * 32, sr + cc * 32, red[cc]);
       } else if (!need_mask) {
 #pragma unroll
-        for (int cc = 0; cc < kWideBN / 32; ++cc)
+        for (int cc = 0; cc < BN / 32; ++cc)
           tmem_ld32_min(s_addr + cc * 32, sr + cc * 32, red[cc]);
       } else {
 #pragma unroll
-        for (int cc = 0; cc < kWideBN / 32; ++cc) {
+        for (int cc = 0; cc < BN / 32; ++cc) {
           tmem_ld32(s_addr + cc * 32, sr + cc * 32);
           red[cc] = 0.f;
         }
       }
       tmem_ld_wait();
 #pragma unroll
-      for (int cc = 0; cc < kWideBN / 32; ++cc) {
+      for (int cc = 0; cc < BN / 32; ++cc) {
         reg_fence32(sr + cc * 32);
         reg_fence_f(red[cc]);
       }
 #define S_(i) __uint_as_float(sr[(i)])
       // ---- row extreme over the visible keys of this block ----
-      int n_vis = kWideBN;
+      int n_vis = BN;
       if (need_mask) {
         int lim = p.Nkv - col0;
         if (CAUSAL) lim = min(lim, q_abs - col0 + 1);
-        n_vis = max(0, min(kWideBN, lim));
+        n_vis = max(0, min(BN, lim));
       }
       float ext;
       if (!need_mask) {
-        ext = neg_scale ? fminf(red[0], red[1]) : fmaxf(red[0], red[1]);
+        ext = red[0];
+#pragma unroll
+        for (int cc = 1; cc < BN / 32; ++cc)
+          ext = neg_scale ? fminf(ext, red[cc]) : fmaxf(ext, red[cc]);
       } else {
         ext = neg_scale ? INFINITY : -INFINITY;
 #pragma unroll
-        for (int i = 0; i < kWideBN; ++i)
+        for (int i = 0; i < BN; ++i)
           if (i < n_vis) ext = neg_scale ? fminf(ext, S_(i)) : fmaxf(ext, S_(i));
       }
       const float m_blk = (n_vis > 0) ? ext * c : -INFINITY;
@@ -321,14 +327,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
 
       // ---- P = exp2(s * c - m), row sum, pack to bf16 ----
-      uint32_t pp[kWideBN / 2];
+      uint32_t pp[BN / 2];
       float rsum;
       if (!need_mask) {
         const uint64_t c2 = f2(c, c);
         const uint64_t nm2 = f2(-m_use, -m_use);
         uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int i = 0; i < kWideBN; i += 2) {
+        for (int i = 0; i < BN; i += 2) {
           float x0, x1;
           f2_split(fma2(f2(S_(i), S_(i + 1)), c2, nm2), x0, x1);
           const float e0 = ex2_approx(x0);
@@ -342,7 +348,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       } else {
         float r[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < kWideBN; i += 2) {
+        for (int i = 0; i < BN; i += 2) {
           const float e0 = (i < n_vis) ? ex2_approx(fmaf(S_(i), c, -m_use)) : 0.f;
           const float e1 =
               (i + 1 < n_vis) ? ex2_approx(fmaf(S_(i + 1), c, -m_use)) : 0.f;
@@ -354,7 +360,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 #undef S_
       l_run = l_run * alpha + rsum;
       m_ref = m_new;
-      tmem_st32(tmem + lane_off + static_cast<uint32_t>(u * kWideBN), pp);
+      tmem_st32(tmem + lane_off + static_cast<uint32_t>(u * BN), pp);
 
       // ---- rescale O when the reference max moved.  PV(j-1) may still be
       // running (S(j) was issued before it), so wait for it first. ----
