@@ -42,8 +42,8 @@ typedef enum {
     FA_ERR_INVALID_VALUE = 1, /* null pointer, dimension < 1, Hq % Hkv != 0,
                                  non-finite scale, size beyond the limits   */
     FA_ERR_UNSUPPORTED = 2,   /* D not in {64, 128, 192, 256}, or the
-                                 current device is
-                                 not compute capability 10.3 (sm_103)       */
+                                 current device is not compute capability
+                                 10.3 (sm_103)                              */
     FA_ERR_MISALIGNED = 3,    /* q, k, v or o not 16-byte aligned, or lse not
                                  4-byte aligned (TMA needs 16 bytes)        */
     FA_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (launch,
