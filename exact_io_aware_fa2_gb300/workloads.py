@@ -117,3 +117,15 @@ def make_custom(B, Hq, Hkv, Nq, Nkv, D, seed=0, q_std=1.0):
     """Seeded N(0,1) bf16 inputs of an arbitrary shape (edge-case tests)."""
     w = Workload("custom", B, Hq, Hkv, Nq, Nkv, D, False, q_std=q_std)
     return make_inputs(w, seed)
+
+
+def make_custom_on_device(B, Hq, Hkv, Nq, Nkv, D, seed=0, device="cuda"):
+    """Seeded N(0,1) bf16 inputs drawn directly on a device, for shapes too
+    large to draw on the host (maximum-size tests).  Q, then K, then V from
+    one generator seeded with ``seed`` on that device."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    out = []
+    for shape in ((B, Hq, Nq, D), (B, Hkv, Nkv, D), (B, Hkv, Nkv, D)):
+        out.append(torch.randn(shape, generator=gen, device=device,
+                               dtype=torch.bfloat16))
+    return tuple(out)
