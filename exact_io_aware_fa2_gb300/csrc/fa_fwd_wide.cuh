@@ -313,10 +313,19 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         for (int cc = 1; cc < BN / 32; ++cc)
           ext = neg_scale ? fminf(ext, red[cc]) : fmaxf(ext, red[cc]);
       } else {
-        ext = neg_scale ? INFINITY : -INFINITY;
+        // four independent chains of three-input extremes over the visible
+        // keys (the others take the identity)
+        const float idn = neg_scale ? INFINITY : -INFINITY;
+        float e4[4] = {idn, idn, idn, idn};
 #pragma unroll
-        for (int i = 0; i < BN; ++i)
-          if (i < n_vis) ext = neg_scale ? fminf(ext, S_(i)) : fmaxf(ext, S_(i));
+        for (int i = 0; i < BN; i += 2) {
+          const float v0 = (i < n_vis) ? S_(i) : idn;
+          const float v1 = (i + 1 < n_vis) ? S_(i + 1) : idn;
+          float& e = e4[(i >> 1) & 3];
+          e = neg_scale ? fmin3(e, v0, v1) : fmax3(e, v0, v1);
+        }
+        ext = neg_scale ? fminf(fminf(e4[0], e4[1]), fminf(e4[2], e4[3]))
+                        : fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]));
       }
       const float m_blk = (n_vis > 0) ? ext * c : -INFINITY;
       const bool move = m_blk > m_ref + kRescaleLog2 ||
@@ -346,16 +355,24 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), s0, s1);
         rsum = s0 + s1;
       } else {
-        float r[4] = {0.f, 0.f, 0.f, 0.f};
+        // the same packed loop; invisible keys get x = -inf, so p = 0
+        const uint64_t c2 = f2(c, c);
+        const uint64_t nm2 = f2(-m_use, -m_use);
+        uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int i = 0; i < BN; i += 2) {
-          const float e0 = (i < n_vis) ? ex2_approx(fmaf(S_(i), c, -m_use)) : 0.f;
-          const float e1 =
-              (i + 1 < n_vis) ? ex2_approx(fmaf(S_(i + 1), c, -m_use)) : 0.f;
-          r[(i >> 1) & 3] += e0 + e1;
+          float x0, x1;
+          f2_split(fma2(f2(S_(i), S_(i + 1)), c2, nm2), x0, x1);
+          x0 = (i < n_vis) ? x0 : -INFINITY;
+          x1 = (i + 1 < n_vis) ? x1 : -INFINITY;
+          const float e0 = ex2_approx(x0);
+          const float e1 = ex2_approx(x1);
+          acc[(i >> 1) & 3] = add2(acc[(i >> 1) & 3], f2(e0, e1));
           pp[i / 2] = pack_bf16x2(e0, e1);
         }
-        rsum = (r[0] + r[1]) + (r[2] + r[3]);
+        float s0, s1;
+        f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), s0, s1);
+        rsum = s0 + s1;
       }
 #undef S_
       l_run = l_run * alpha + rsum;
