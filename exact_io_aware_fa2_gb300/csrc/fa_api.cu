@@ -62,7 +62,11 @@ cudaError_t opt_in_smem() {
 
 template <int D, bool CAUSAL>
 cudaError_t opt_in_smem_wide() {
-  return cudaFuncSetAttribute(fa::fa_fwd_wide_kernel<D, CAUSAL>,
+  cudaError_t e = cudaFuncSetAttribute(
+      fa::fa_fwd_wide_kernel<D, CAUSAL, false>,
+      cudaFuncAttributeMaxDynamicSharedMemorySize, fa::WideCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(fa::fa_fwd_wide_kernel<D, CAUSAL, true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               fa::WideCfg<D>::kSmemBytes);
 }
@@ -150,15 +154,22 @@ constexpr int kMinSplitBlocks = 4;
 constexpr int kMaxSplits = 64;
 constexpr int kSplitOverheadBlocks = 3;
 
-int plan_splits(int B, int Hq, int Nq, int Nkv, int causal, int sms) {
-  const long long pairs = (Nq + fa::kBM * fa::kTilesPerCta - 1) /
-                          (fa::kBM * fa::kTilesPerCta);
-  const long long ctas = pairs * Hq * B;
+// Query rows per CTA and keys per K/V block of the kernel a head dim runs
+// (the two-tile kernel: 256 and 128; the wide-head kernel: 128 and 64).
+int unit_rows(int D) {
+  return wide_head_dim(D) ? fa::kBM : fa::kBM * fa::kTilesPerCta;
+}
+int block_keys(int D) { return wide_head_dim(D) ? 64 : fa::kBN; }
+
+int plan_splits(int B, int Hq, int Nq, int Nkv, int D, int causal, int sms) {
+  const int rows_u = unit_rows(D), keys_b = block_keys(D);
+  const long long units = (Nq + rows_u - 1) / rows_u;
+  const long long ctas = units * Hq * B;
   if (ctas * 2 > sms) return 1;
-  long long longest = (Nkv + fa::kBN - 1) / fa::kBN;     // K/V blocks
+  long long longest = (Nkv + keys_b - 1) / keys_b;       // K/V blocks
   if (causal) {
     const int rows = Nq < Nkv ? Nq : Nkv;
-    longest = (rows + fa::kBN - 1) / fa::kBN;
+    longest = (rows + keys_b - 1) / keys_b;
   }
   long long cap = longest / kMinSplitBlocks;
   if (cap > kMaxSplits) cap = kMaxSplits;
@@ -192,13 +203,14 @@ RunShape run_shape(int Hq, int Hkv, int Nq, int causal) {
   return {Hkv, static_cast<int>(packed)};
 }
 
+// Split-KV scratch: one fp32 slot of unit_rows(D) * (D + 2) words per
+// (batch, head, unit of query rows, K/V range).
 int64_t workspace_bytes(int B, int Hq, int Nq, int D, int splits) {
   if (splits <= 1) return 0;
-  const int64_t pairs = (Nq + fa::kBM * fa::kTilesPerCta - 1) /
-                        (fa::kBM * fa::kTilesPerCta);
-  const int64_t slot = D == 64 ? fa::FwdCfg<64>::kSlotFloats
-                               : fa::FwdCfg<128>::kSlotFloats;
-  return static_cast<int64_t>(B) * Hq * pairs * splits * slot * 4;
+  const int64_t rows_u = unit_rows(D);
+  const int64_t units = (Nq + rows_u - 1) / rows_u;
+  const int64_t slot = rows_u * (D + 2);
+  return static_cast<int64_t>(B) * Hq * units * splits * slot * 4;
 }
 
 // Tensor map of a contiguous bf16 [BH, N, D] tensor, read in boxes of 64
@@ -224,6 +236,17 @@ int encode_bhnd(CUtensorMap* map, const void* ptr, long long BH, int N,
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// fa_merge_kernel over units of ROWS query rows.
+template <int D, int ROWS>
+int launch_merge(const fa::FwdParams& p, int B, int Hq, int Nq,
+                 cudaStream_t stream) {
+  using M = fa::MergeCfg<D>;
+  const int units = (Nq + ROWS - 1) / ROWS;
+  dim3 mgrid(units * (ROWS / M::kRowsPerBlock), Hq, B);
+  fa::fa_merge_kernel<D, ROWS><<<mgrid, M::kThreads, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 template <int D, bool CAUSAL>
 int launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
            const fa::FwdParams& p, int B, int Hq, int Nq,
@@ -240,12 +263,8 @@ int launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
         <<<grid, fa::kThreads, fa::FwdCfg<D>::kSmemBytes, stream>>>(q, k, v,
                                                                      p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  if (p.kv_splits > 1) {
-    constexpr int kRowsPerBlock = 256 / (D / 4);
-    dim3 mgrid(pairs * (rows_per_cta / kRowsPerBlock), Hq, B);
-    fa::fa_merge_kernel<D><<<mgrid, 256, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  }
+  if (p.kv_splits > 1) return launch_merge<D, fa::kBM * fa::kTilesPerCta>(
+                                p, B, Hq, Nq, stream);
   return FA_OK;
 }
 
@@ -253,11 +272,19 @@ template <int D, bool CAUSAL>
 int launch_wide(const CUtensorMap& q, const CUtensorMap& k,
                 const CUtensorMap& v, const fa::FwdParams& p, int B, int Hq,
                 int Nq, cudaStream_t stream) {
-  dim3 grid((Nq + fa::kBM - 1) / fa::kBM, Hq, B);
-  fa::fa_fwd_wide_kernel<D, CAUSAL>
-      <<<grid, fa::kWideThreads, fa::WideCfg<D>::kSmemBytes, stream>>>(q, k, v,
-                                                                       p);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  dim3 grid((Nq + fa::kBM - 1) / fa::kBM, Hq, B * p.kv_splits);
+  if (p.kv_splits > 1)
+    fa::fa_fwd_wide_kernel<D, CAUSAL, true>
+        <<<grid, fa::kWideThreads, fa::WideCfg<D>::kSmemBytes, stream>>>(
+            q, k, v, p);
+  else
+    fa::fa_fwd_wide_kernel<D, CAUSAL, false>
+        <<<grid, fa::kWideThreads, fa::WideCfg<D>::kSmemBytes, stream>>>(
+            q, k, v, p);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  if (p.kv_splits > 1)
+    return launch_merge<D, fa::kBM>(p, B, Hq, Nq, stream);
+  return FA_OK;
 }
 
 bool aligned(const void* p, uintptr_t a) {
@@ -323,10 +350,7 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
                                     1.4426950408889634074);
   p.status = word;
   p.wait_limit_ns = kWaitLimitNs;
-  // The wide-head kernel has no split-KV form.
-  p.kv_splits = wide_head_dim(D)
-                    ? 1
-                    : plan_splits(B, Hq, Nq, Nkv, causal, g_sm_count[dev]);
+  p.kv_splits = plan_splits(B, Hq, Nq, Nkv, D, causal, g_sm_count[dev]);
   p.work = nullptr;
   const int64_t need = workspace_bytes(B, Hq, Nq, D, p.kv_splits);
   void* owned = nullptr;
@@ -408,9 +432,7 @@ int fa_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
   const RunShape rs = run_shape(Hq, Hkv, Nq, causal);
   *bytes = static_cast<size_t>(workspace_bytes(
       B, rs.Hq, rs.Nq, D,
-      wide_head_dim(D)
-          ? 1
-          : plan_splits(B, rs.Hq, rs.Nq, Nkv, causal, g_sm_count[dev])));
+      plan_splits(B, rs.Hq, rs.Nq, Nkv, D, causal, g_sm_count[dev])));
   return FA_OK;
 }
 

@@ -578,40 +578,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 // m_s, log2 domain) and l_s; with m = max_s m_s
 //     l = sum_s l_s 2^(m_s - m),   O = sum_s O_s 2^(m_s - m) / l,
 //     LSE = (m + log2 l) ln 2,
-// the same rescaling the online softmax applies between K/V blocks.  One
-// thread per (row, 4 columns); grid (pairs * 256 / rows-per-block, Hq, B).
+// the same rescaling the online softmax applies between K/V blocks.  A
+// partial slot covers one unit of ROWS query rows (a tile pair of the
+// two-tile kernel, a tile of the wide-head kernel): fp32 O [ROWS][D], then
+// m [ROWS], then l [ROWS].  One thread per (row, 4 columns).
 template <int D>
-__global__ void __launch_bounds__(256)
+struct MergeCfg {
+  static constexpr int kChunks = D / 4;           // float4 per row
+  static constexpr int kRowsPerBlock = (D == 64) ? 16 : (D == 128) ? 8 : 4;
+  static constexpr int kThreads = kRowsPerBlock * kChunks;
+};
+
+template <int D, int ROWS>
+__global__ void __launch_bounds__(MergeCfg<D>::kThreads)
     fa_merge_kernel(const __grid_constant__ FwdParams p) {
-  using C = FwdCfg<D>;
-  constexpr int kRows = kTilesPerCta * kBM;       // rows of a pair
-  constexpr int kChunks = D / 4;                  // float4 per row
-  constexpr int kRowsPerBlock = 256 / kChunks;
+  using M = MergeCfg<D>;
+  constexpr int64_t kSlot = static_cast<int64_t>(ROWS) * (D + 2);
   const int splits = p.kv_splits;
-  const int blocks_per_pair = kRows / kRowsPerBlock;
-  const int pair = static_cast<int>(blockIdx.x) / blocks_per_pair;
-  const int prow = (static_cast<int>(blockIdx.x) % blocks_per_pair) *
-                       kRowsPerBlock +
-                   static_cast<int>(threadIdx.x) / kChunks;
-  const int ch = static_cast<int>(threadIdx.x) % kChunks;
+  constexpr int kBlocksPerUnit = ROWS / M::kRowsPerBlock;
+  const int unit = static_cast<int>(blockIdx.x) / kBlocksPerUnit;
+  const int prow = (static_cast<int>(blockIdx.x) % kBlocksPerUnit) *
+                       M::kRowsPerBlock +
+                   static_cast<int>(threadIdx.x) / M::kChunks;
+  const int ch = static_cast<int>(threadIdx.x) % M::kChunks;
   const int hq = blockIdx.y, b = blockIdx.z;
-  const int q_row = pair * kRows + prow;
+  const int q_row = unit * ROWS + prow;
   if (q_row >= p.Nq) return;
-  const int n_pairs = (p.Nq + kRows - 1) / kRows;
+  const int n_units = (p.Nq + ROWS - 1) / ROWS;
   const float* base = p.work + ((static_cast<int64_t>(b) * p.Hq + hq) *
-                                    n_pairs + pair) * splits * C::kSlotFloats;
+                                    n_units + unit) * splits * kSlot;
   float m = -INFINITY;
   for (int s = 0; s < splits; ++s)
-    m = fmaxf(m, base[s * C::kSlotFloats + kRows * D + prow]);
+    m = fmaxf(m, base[s * kSlot + ROWS * D + prow]);
   float l = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
   for (int s = 0; s < splits; ++s) {
-    const float* slot = base + s * C::kSlotFloats;
-    const float ms = slot[kRows * D + prow];
+    const float* slot = base + s * kSlot;
+    const float ms = slot[ROWS * D + prow];
     if (ms == -INFINITY) continue;                // range saw no key
     const float w = ex2_approx(ms - m);
-    l += slot[kRows * D + kRows + prow] * w;
+    l += slot[ROWS * D + ROWS + prow] * w;
     const float4 o = reinterpret_cast<const float4*>(slot + prow * D)[ch];
     acc.x += o.x * w;
     acc.y += o.y * w;

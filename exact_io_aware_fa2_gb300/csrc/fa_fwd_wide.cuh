@@ -62,6 +62,9 @@ struct WideCfg {
                                     (kKStages + kVStages) * kKVBytes +
                                     kBarBytes;
   static constexpr uint32_t kColO = 2 * kBN;
+  // fp32 words of one split-KV partial slot: O rows [128][D] (unnormalised,
+  // relative to the slot's reference max), then m[128], then l[128].
+  static constexpr int64_t kSlotFloats = static_cast<int64_t>(kBM) * (D + 2);
   static constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);
 };
@@ -100,7 +103,10 @@ __device__ __forceinline__ void wide_issue_pv(uint32_t d_tmem, uint32_t a_tmem,
                  dv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc);
 }
 
-template <int D, bool CAUSAL>
+// SPLIT: the grid's z index also carries a K/V range (split-KV); the CTA
+// then processes that range of its tile's blocks and leaves fp32 partials
+// for fa_merge_kernel<D, 128>.
+template <int D, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(kWideThreads, 1)
     fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
@@ -120,11 +126,19 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const int tile = CAUSAL ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
                           : static_cast<int>(blockIdx.x);
   const int hq = blockIdx.y;
-  const int b = blockIdx.z;
+  const int splits = SPLIT ? p.kv_splits : 1;
+  const int b = SPLIT ? static_cast<int>(blockIdx.z) / splits
+                      : static_cast<int>(blockIdx.z);
+  const int split = SPLIT ? static_cast<int>(blockIdx.z) - b * splits : 0;
   const int hk = hq / (p.Hq / p.Hkv);
   const int row0 = tile * kBM;
   const int kv_end = CAUSAL ? min(p.Nkv, row0 + kBM) : p.Nkv;
-  const int nblk = (kv_end + BN - 1) / BN;
+  const int nblk_tile = (kv_end + BN - 1) / BN;
+  // This CTA's contiguous range [j0, j0 + nblk) of the tile's K/V blocks
+  // (all of them without split-KV; possibly none for a short causal tile).
+  const int chunk = SPLIT ? (nblk_tile + splits - 1) / splits : nblk_tile;
+  const int j0 = SPLIT ? min(nblk_tile, split * chunk) : 0;
+  const int nblk = SPLIT ? min(nblk_tile, j0 + chunk) - j0 : nblk_tile;
 
   // ---- shared memory (1024-byte aligned for the swizzle atoms) ----
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -202,13 +216,13 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         mbar_arrive_expect_tx(bKFull(sk), W::kKVBytes);
         for (int c = 0; c < W::kBoxes; ++c)
           tma_load_3d(sK + sk * W::kKVBytes + c * W::kKVBoxBytes, &tmK,
-                      bKFull(sk), c * kBoxCols, j * BN, zk, keep);
+                      bKFull(sk), c * kBoxCols, (j0 + j) * BN, zk, keep);
         k_issued = j + 1;
         if (!mbar_wait(bVEmpty(sv), ((j / NV) & 1) ^ 1, wc)) break;
         mbar_arrive_expect_tx(bVFull(sv), W::kKVBytes);
         for (int c = 0; c < W::kBoxes; ++c)
           tma_load_3d(sV + sv * W::kKVBytes + c * W::kKVBoxBytes, &tmV,
-                      bVFull(sv), c * kBoxCols, j * BN, zk, keep);
+                      bVFull(sv), c * kBoxCols, (j0 + j) * BN, zk, keep);
         v_issued = j + 1;
       }
       // Never leave the CTA with copies in flight.
@@ -273,7 +287,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       uint32_t sr[BN];
       const uint32_t s_addr =
           tmem + lane_off + static_cast<uint32_t>(u * BN);
-      const int col0 = j * BN;
+      const int col0 = (j0 + j) * BN;
       const bool need_mask =
           (col0 + BN > p.Nkv) || (CAUSAL && col0 + BN - 1 > row0);
       float red[BN / 32];
@@ -405,9 +419,37 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       if (lane == 0) mbar_arrive(bPFull(u));
     }
 
-    // ---- epilogue: O / l -> bf16, LSE ----
+    // ---- epilogue ----
     if (ok && nblk > 0) ok = __all_sync(kAll, mbar_wait(bOFinal, 0, wc));
-    if (ok && nblk > 0) {
+    const int trow = (warp & 3) * 32 + lane;         // row within the tile
+    const uint32_t o_addr = tmem + lane_off + W::kColO;
+    if constexpr (SPLIT) {
+      // Partial of one K/V range: unnormalised O (relative to m_ref), m and
+      // l per row.  An empty range leaves m = -inf, l = 0.
+      float* slot = p.work + ((static_cast<int64_t>(b) * p.Hq + hq) *
+                                  static_cast<int64_t>(gridDim.x) +
+                              tile) * splits * W::kSlotFloats +
+                    static_cast<int64_t>(split) * W::kSlotFloats;
+      if (ok && nblk > 0) {
+        tc_fence_after();
+        float4* orow = reinterpret_cast<float4*>(slot + trow * D);
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t orr[32];
+          tmem_ld32(o_addr + cc * 32, orr);
+          tmem_ld_wait();
+          reg_fence32(orr);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            orow[cc * 8 + i] = make_float4(
+                __uint_as_float(orr[4 * i]), __uint_as_float(orr[4 * i + 1]),
+                __uint_as_float(orr[4 * i + 2]),
+                __uint_as_float(orr[4 * i + 3]));
+        }
+      }
+      slot[kBM * D + trow] = nblk > 0 ? m_ref : -INFINITY;
+      slot[kBM * D + kBM + trow] = nblk > 0 ? l_run : 0.f;
+    } else if (ok && nblk > 0) {
       tc_fence_after();
       const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
       const bool in_range = q_abs < p.Nq;
@@ -415,7 +457,6 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           (static_cast<size_t>(b) * p.Hq + hq) * static_cast<size_t>(p.Nq) +
           static_cast<size_t>(q_abs);
       __nv_bfloat16* orow = p.o + row_idx * D;
-      const uint32_t o_addr = tmem + lane_off + W::kColO;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t orr[32];

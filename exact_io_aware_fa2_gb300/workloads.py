@@ -81,6 +81,10 @@ WORKLOADS = {
                  False),
         Workload("wide_causal_b1_h8_n8192_d256", 1, 8, 8, 8192, 8192, 256,
                  True),
+        # The decode/prefill-chunk shape with wide heads: split-KV on the
+        # one-tile kernel.
+        Workload("splitkv_b1_hq32_hkv8_q128_kv32768_d256", 1, 32, 8, 128,
+                 32768, 256, False),
     ]
 }
 

@@ -267,9 +267,34 @@ def test_wide_heads_gqa_batched_large_logits(D):
                        f"wide D{D} GQA large logits"))
 
 
-def test_wide_heads_need_no_workspace():
-    assert fa.workspace_size(1, 8, 8, 128, 32768, 256, False) == 0
-    assert fa.workspace_size(1, 8, 2, 1, 4096, 192, False) == 0
+def test_wide_heads_split_kv_for_few_tiles():
+    # few 128-row tiles over long keys: split-KV
+    assert fa.workspace_size(1, 8, 8, 128, 32768, 256, False) > 0
+    assert fa.workspace_size(1, 8, 2, 1, 4096, 192, False) > 0
+    # enough tiles to fill the GPU: no split
+    assert fa.workspace_size(1, 8, 8, 4096, 8192, 256, False) == 0
+
+
+@pytest.mark.parametrize("D", [192, 256])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nkv", [(1, 2, 1, 64, 5000),
+                                              (1, 2, 1, 600, 3000),
+                                              (2, 4, 2, 1, 4097)])
+def test_wide_heads_split_kv_full(D, causal, B, Hq, Hkv, Nq, Nkv):
+    """Wide heads with few query tiles split the keys: partials per K/V
+    range, then the merge; compared with the oracle everywhere."""
+    q, k, v = make_custom(B, Hq, Hkv, Nq, Nkv, D, seed=D + Nq + Nkv)
+    print(full_compare(q, k, v, 1.0 / math.sqrt(D), causal,
+                       f"wide split D{D} c{causal} {B}x{Hq}/{Hkv} "
+                       f"{Nq}x{Nkv}"))
+
+
+def test_wide_heads_split_kv_large_logits():
+    q, k, v = make_custom(1, 8, 2, 100, 6000, 256, seed=41, q_std=3.0)
+    k[:, :, ::97] *= 8
+    print(full_compare(q, k, v, 1.0 / 16.0, False, "wide split large logits"))
+    print(full_compare(q, k, v, 1.0 / 16.0, True,
+                       "wide split large logits causal"))
 
 
 def test_pool_scratch_and_caller_workspace_agree():
