@@ -41,7 +41,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from exact_io_aware_fa2_gb300.workloads import (HEADLINE, WORKLOADS,  # noqa
-                                                make_inputs)
+                                                make_inputs, quantize_e4m3)
 
 METRIC = ("attention fwd TFLOPS (4·B·H·Nq·Nkv·D, "
           "causal ½) and % of GB300 BF16 peak")
@@ -329,6 +329,10 @@ def sdpa_column(w, q, k, v, o_ours, flush, stream, steps, warmup=5):
         except Exception as exc:  # a backend this GPU/torch cannot run
             entry = {"unavailable": f"{type(exc).__name__}: "
                                     f"{str(exc).splitlines()[0][:160]}"}
+        if w.qk8 and "unavailable" not in entry:
+            entry["note"] = (entry.get("note", "") +
+                             " bf16 Q/K/V: torch SDPA takes no e4m3 inputs"
+                             ).strip()
         out[name.lower()] = entry
     return out
 
@@ -349,9 +353,17 @@ def run_ours(args, w):
     o = torch.empty_like(q)
     lse = torch.empty(w.B, w.Hq, w.Nq, dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    if w.qk8:
+        # e4m3 Q and K with per-tensor descales (the fa_fwd_qk8 path)
+        (q8_h, qd), (k8_h, kd) = quantize_e4m3(q_h), quantize_e4m3(k_h)
+        q8, k8 = q8_h.to(dev), k8_h.to(dev)
 
     def launch():
-        fa.fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse)
+        if w.qk8:
+            fa.fwd_qk8(q8, k8, v, scale=w.scale, q_descale=qd, k_descale=kd,
+                       causal=w.causal, out=o, lse=lse)
+        else:
+            fa.fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse)
 
     for _ in range(max(3, args.warmup)):
         launch()
@@ -389,6 +401,13 @@ def run_ours(args, w):
     value = job_tflops(w.flops, ms_max, ws)
     per_launch_tflops = w.flops / (ms * 1e-3) / 1e12
     peak, peak_src = peaks()
+    peak_src += ", of measured" if "MEASURED" in peak_src else ", of fallback"
+    if w.qk8:
+        # Half the flops (Q K^T) run as e4m3 products at twice the bf16 rate
+        # (the nominal 4.5 vs 2.25 PFLOP/s), half (P V) at the bf16 rate:
+        # the step's peak is 2 / (1/(2P) + 1/P) = 4P/3.
+        peak *= 4.0 / 3.0
+        peak_src += "; x4/3: QK^T at the e4m3 rate (2x bf16), PV at bf16"
     # A split-KV step is the forward kernel plus the merge; the step time
     # (both kernels) then stands for the forward kernel's, a lower bound.
     split = fa.workspace_size(w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D,
@@ -396,18 +415,40 @@ def run_ours(args, w):
     launches_per_step = 2 if split else 1
 
     # ---- end to end through the public API with host buffers ----
-    qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
-    bufs = fa.host_buffers(qp, kp, vp, device=dev)
+    if w.qk8:
+        host_in = (q8_h, k8_h, v_h)
+        pinned = [t.pin_memory() for t in host_in]
+        dev_in = [torch.empty_like(t, device=dev) for t in host_in]
+        o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+        def e2e_step():
+            for d_, h_ in zip(dev_in, pinned):
+                d_.copy_(h_, non_blocking=True)
+            fa.fwd_qk8(dev_in[0], dev_in[1], dev_in[2], scale=w.scale,
+                       q_descale=qd, k_descale=kd, causal=w.causal, out=o,
+                       lse=lse)
+            o_h.copy_(o, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+    else:
+        host_in = (q_h, k_h, v_h)
+        qp, kp, vp = (t.pin_memory() for t in host_in)
+        bufs = fa.host_buffers(qp, kp, vp, device=dev)
+
+        def e2e_step():
+            fa.fwd_host(qp, kp, vp, scale=w.scale, causal=w.causal,
+                        bufs=bufs)
     for _ in range(3):
-        fa.fwd_host(qp, kp, vp, scale=w.scale, causal=w.causal, bufs=bufs)
+        e2e_step()
     e2e_steps = max(5, min(args.steps, 50))
     barrier()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        fa.fwd_host(qp, kp, vp, scale=w.scale, causal=w.causal, bufs=bufs)
+        e2e_step()
     barrier()
     e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, dev)
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
 
     sdpa = None
@@ -427,7 +468,8 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
+        "dtype": "e4m3 QK^T, bf16 PV" if w.qk8 else "bf16",
+        "data": "synthetic",
         "pct_of_peak": 100.0 * per_launch_tflops / peak,
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
                    "Nq": w.Nq, "Nkv": w.Nkv, "D": w.D, "causal": w.causal,
@@ -438,8 +480,7 @@ def run_ours(args, w):
         "roofline": {"bound": "tensor", "achieved": per_launch_tflops,
                      "peak": peak, "unit": "TFLOP/s",
                      "frac": per_launch_tflops / peak,
-                     "peak_source": peak_src + ", of measured"
-                     if "MEASURED" in peak_src else peak_src + ", of fallback",
+                     "peak_source": peak_src,
                      "traffic": recorded_traffic(w),
                      "kernel": "fa_fwd_kernel<SPLIT> + fa_merge_kernel"
                      if split else kernel_for(w),

@@ -49,15 +49,16 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool QK8 = false>
 cudaError_t opt_in_smem() {
+  constexpr int kSmem = fa::FwdCfg<D, QK8>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(
-      fa::fa_fwd_kernel<D, CAUSAL, false>,
-      cudaFuncAttributeMaxDynamicSharedMemorySize, fa::FwdCfg<D>::kSmemBytes);
+      fa::fa_fwd_kernel<D, CAUSAL, false, QK8>,
+      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, true>,
+  return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, true, QK8>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              fa::FwdCfg<D>::kSmemBytes);
+                              kSmem);
 }
 
 template <int D, bool CAUSAL>
@@ -109,6 +110,8 @@ int device_ready(int** word_out, int* dev_out = nullptr) {
         opt_in_smem<64, true>() != cudaSuccess ||
         opt_in_smem<128, false>() != cudaSuccess ||
         opt_in_smem<128, true>() != cudaSuccess ||
+        opt_in_smem<128, false, true>() != cudaSuccess ||
+        opt_in_smem<128, true, true>() != cudaSuccess ||
         opt_in_smem_wide<192, false>() != cudaSuccess ||
         opt_in_smem_wide<192, true>() != cudaSuccess ||
         opt_in_smem_wide<256, false>() != cudaSuccess ||
@@ -236,6 +239,27 @@ int encode_bhnd(CUtensorMap* map, const void* ptr, long long BH, int N,
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// The same for a one-byte (e4m3) [BH, N, D] tensor: boxes of 128 head-dim
+// elements (one 128-byte swizzle row) by 128 sequence rows.
+int encode_bhnd_e4m3(CUtensorMap* map, const void* ptr, long long BH, int N,
+                     int D) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return FA_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D),
+                        static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D),
+                           static_cast<cuuint64_t>(N) * D};
+  cuuint32_t box[3] = {128u, static_cast<cuuint32_t>(fa::kBM), 1};
+  cuuint32_t elem_strides[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                   const_cast<void*>(ptr), dims, strides, box, elem_strides,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 // fa_merge_kernel over units of ROWS query rows.
 template <int D, int ROWS>
 int launch_merge(const fa::FwdParams& p, int B, int Hq, int Nq,
@@ -247,21 +271,20 @@ int launch_merge(const fa::FwdParams& p, int B, int Hq, int Nq,
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool QK8 = false>
 int launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
            const fa::FwdParams& p, int B, int Hq, int Nq,
            cudaStream_t stream) {
+  constexpr int kSmem = fa::FwdCfg<D, QK8>::kSmemBytes;
   const int rows_per_cta = fa::kBM * fa::kTilesPerCta;
   const int pairs = (Nq + rows_per_cta - 1) / rows_per_cta;
   dim3 grid(pairs, Hq, B * p.kv_splits);
   if (p.kv_splits > 1)
-    fa::fa_fwd_kernel<D, CAUSAL, true>
-        <<<grid, fa::kThreads, fa::FwdCfg<D>::kSmemBytes, stream>>>(q, k, v,
-                                                                     p);
+    fa::fa_fwd_kernel<D, CAUSAL, true, QK8>
+        <<<grid, fa::kThreads, kSmem, stream>>>(q, k, v, p);
   else
-    fa::fa_fwd_kernel<D, CAUSAL, false>
-        <<<grid, fa::kThreads, fa::FwdCfg<D>::kSmemBytes, stream>>>(q, k, v,
-                                                                     p);
+    fa::fa_fwd_kernel<D, CAUSAL, false, QK8>
+        <<<grid, fa::kThreads, kSmem, stream>>>(q, k, v, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   if (p.kv_splits > 1) return launch_merge<D, fa::kBM * fa::kTilesPerCta>(
                                 p, B, Hq, Nq, stream);
@@ -326,12 +349,21 @@ int check_args(const void* q, const void* k, const void* v, const void* o,
 
 // Shared body of fa_fwd and fa_fwd_ws.  Scratch: from the device pool when
 // `pool_scratch`, else the caller's `workspace` (`ws_bytes` long).
+// `qk8`: q and k are e4m3 with descale factors q_descale and k_descale
+// (D = 128 only); the scores are then (q k^T) * q_descale * k_descale.
 int run_forward(const void* q, const void* k, const void* v, void* o,
                 float* lse, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
                 float scale, int causal, void* workspace, size_t ws_bytes,
-                bool pool_scratch, cudaStream_t s) {
+                bool pool_scratch, cudaStream_t s, bool qk8 = false,
+                float q_descale = 1.f, float k_descale = 1.f) {
   int st = check_args(q, k, v, o, lse, B, Hq, Hkv, Nq, Nkv, D, scale);
   if (st != FA_OK) return st;
+  if (qk8) {
+    if (!std::isfinite(q_descale) || !std::isfinite(k_descale) ||
+        !(q_descale > 0.f) || !(k_descale > 0.f))
+      return FA_ERR_INVALID_VALUE;
+    if (D != 128) return FA_ERR_UNSUPPORTED;
+  }
   int* word = nullptr;
   int dev = 0;
   if ((st = device_ready(&word, &dev)) != FA_OK) return st;
@@ -346,8 +378,9 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
   p.Nkv = Nkv;
   p.Hq = Hq;
   p.Hkv = Hkv;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) *
-                                    1.4426950408889634074);
+  p.scale_log2 = static_cast<float>(
+      static_cast<double>(scale) * 1.4426950408889634074 *
+      (qk8 ? static_cast<double>(q_descale) * k_descale : 1.0));
   p.status = word;
   p.wait_limit_ns = kWaitLimitNs;
   p.kv_splits = plan_splits(B, Hq, Nq, Nkv, D, causal, g_sm_count[dev]);
@@ -372,15 +405,25 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
   const int kv_rows = !wide_head_dim(D) ? fa::kBN
                       : D == 192          ? fa::WideCfg<192>::kBN
                                           : fa::WideCfg<256>::kBN;
-  if ((st = encode_bhnd(&tq, q, static_cast<long long>(B) * Hq, Nq, D)) ||
-      (st = encode_bhnd(&tk, k, static_cast<long long>(B) * Hkv, Nkv, D,
-                        kv_rows)) ||
+  const bool qk_ok =
+      qk8 ? (encode_bhnd_e4m3(&tq, q, static_cast<long long>(B) * Hq, Nq,
+                              D) == FA_OK &&
+             encode_bhnd_e4m3(&tk, k, static_cast<long long>(B) * Hkv, Nkv,
+                              D) == FA_OK)
+          : (encode_bhnd(&tq, q, static_cast<long long>(B) * Hq, Nq, D) ==
+                 FA_OK &&
+             encode_bhnd(&tk, k, static_cast<long long>(B) * Hkv, Nkv, D,
+                         kv_rows) == FA_OK);
+  if ((st = qk_ok ? FA_OK : FA_ERR_CUDA) ||
       (st = encode_bhnd(&tv, v, static_cast<long long>(B) * Hkv, Nkv, D,
                         kv_rows))) {
     if (owned != nullptr) cudaFreeAsync(owned, s);
     return st;
   }
-  if (D == 256)
+  if (qk8)
+    st = causal ? launch<128, true, true>(tq, tk, tv, p, B, Hq, Nq, s)
+                : launch<128, false, true>(tq, tk, tv, p, B, Hq, Nq, s);
+  else if (D == 256)
     st = causal ? launch_wide<256, true>(tq, tk, tv, p, B, Hq, Nq, s)
                 : launch_wide<256, false>(tq, tk, tv, p, B, Hq, Nq, s);
   else if (D == 192)
@@ -416,6 +459,15 @@ int fa_fwd_ws(const void* q, const void* k, const void* v, void* o,
   return run_forward(q, k, v, o, lse, B, Hq, Hkv, Nq, Nkv, D, scale, causal,
                      workspace, workspace_bytes_, false,
                      static_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd_qk8(const void* q8, const void* k8, const void* v, void* o,
+               float* lse, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+               float scale, float q_descale, float k_descale, int causal,
+               void* stream) {
+  return run_forward(q8, k8, v, o, lse, B, Hq, Hkv, Nq, Nkv, D, scale, causal,
+                     nullptr, 0, true, static_cast<cudaStream_t>(stream),
+                     true, q_descale, k_descale);
 }
 
 int fa_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int D,

@@ -63,15 +63,23 @@ constexpr int kSoftmaxWarp0 = 2;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr uint32_t kTmemCols = 512;
 
-template <int D>
+// QK8: Q and K are e4m3 (one byte per element) and S = Q K^T runs as
+// kind::f8f6f4; V, P and O stay as without it.
+template <int D, bool QK8 = false>
 struct FwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
+  static_assert(!QK8 || D == 128, "e4m3 Q/K at head dim 128 only");
   static constexpr int kTileBytes = kBM * D * 2;       // 16 KiB or 32 KiB
   static constexpr int kBoxes = D / kBoxCols;          // TMA boxes per tile
+  // Q and K tiles: a 128-byte swizzle row holds 64 bf16 or 128 e4m3.
+  static constexpr int kQKElemBytes = QK8 ? 1 : 2;
+  static constexpr int kQKBoxCols = 128 / kQKElemBytes;
+  static constexpr int kQKBoxes = D / kQKBoxCols;
+  static constexpr int kQKTileBytes = kBM * D * kQKElemBytes;
   // Ring depths.  V_j is released one MMA group later than K_j (after the
   // second tile's P*V rather than its S), so V gets the deeper ring: both
   // loads are then issued two iterations ahead of their use.
-  static constexpr int kKStages = (D == 128) ? 2 : 4;
+  static constexpr int kKStages = (D == 128) ? (QK8 ? 4 : 2) : 4;
   static constexpr int kVStages = (D == 128) ? 3 : 4;
   // barriers: Q, K full/empty, V full/empty, S full x2, P full x2, O final,
   // drain
@@ -80,7 +88,8 @@ struct FwdCfg {
   static constexpr int kBarBytes = 8 * kNumBars + 32;
   static constexpr int kSmemBytes =
       1024 /*alignment slack*/ +
-      kTileBytes * (kTilesPerCta + kKStages + kVStages) + kBarBytes;
+      kQKTileBytes * (kTilesPerCta + kKStages) + kTileBytes * kVStages +
+      kBarBytes;
   // TMEM column of tile x's S, O and P.
   __host__ __device__ static constexpr uint32_t col_s(int x) {
     return x ? 128u : 0u;
@@ -91,7 +100,8 @@ struct FwdCfg {
   __host__ __device__ static constexpr uint32_t col_p(int x) {
     return D == 128 ? col_s(x) : (x ? 448u : 384u);
   }
-  static constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
+  static constexpr uint32_t kIdescS = QK8 ? idesc_e4m3_f32(kBM, kBN)
+                                          : idesc_bf16_f32(kBM, kBN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);
   // fp32 words of one partial slot: O rows [256][D] (unnormalised, relative
   // to the slot's reference max), then m[256] (log2 domain), then l[256].
@@ -118,15 +128,25 @@ struct FwdParams {
 // moves the start address 32 bytes within a swizzle row, and every 64
 // elements to the next TMA box.  Offsets are compile-time constants added to
 // the start-address field of prebuilt descriptors.
-template <int D>
+template <int D, bool QK8>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dq,
                                          uint64_t dk, uint32_t idesc) {
-  mma_ss_w<0>(d_tmem, dq, dk, idesc);
+  if constexpr (QK8) {
+    // e4m3: K = 32 elements (32 bytes) per MMA, D / 32 MMAs in one box
+    mma_ss8_w<0>(d_tmem, dq, dk, idesc);
 #pragma unroll
-  for (int kk = 1; kk < D / 16; ++kk) {
-    const uint64_t off = static_cast<uint64_t>(
-        ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
-    mma_ss_w<1>(d_tmem, dq + off, dk + off, idesc);
+    for (int kk = 1; kk < D / 32; ++kk) {
+      const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
+      mma_ss8_w<1>(d_tmem, dq + off, dk + off, idesc);
+    }
+  } else {
+    mma_ss_w<0>(d_tmem, dq, dk, idesc);
+#pragma unroll
+    for (int kk = 1; kk < D / 16; ++kk) {
+      const uint64_t off = static_cast<uint64_t>(
+          ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+      mma_ss_w<1>(d_tmem, dq + off, dk + off, idesc);
+    }
   }
 }
 
@@ -155,13 +175,13 @@ __device__ __forceinline__ int kv_blocks(int row0, int Nkv) {
 // SPLIT: the grid's z index also carries the K/V range (split-KV) and the
 // epilogue writes fp32 partials; without it the code is the plain one-pair-
 // per-CTA forward.
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, bool CAUSAL, bool SPLIT, bool QK8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, QK8>;
   constexpr int NK = C::kKStages;
   constexpr int NV = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
@@ -194,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - smem_addr(smem_raw));
   const uint32_t sQ = base;                          // Q_A, then Q_B
-  const uint32_t sK = sQ + kTilesPerCta * C::kTileBytes;
-  const uint32_t sV = sK + NK * C::kTileBytes;
+  const uint32_t sK = sQ + kTilesPerCta * C::kQKTileBytes;
+  const uint32_t sV = sK + NK * C::kQKTileBytes;
   const uint32_t sBar = sV + NV * C::kTileBytes;
   auto bar = [&](int i) { return sBar + 8u * static_cast<uint32_t>(i); };
   const uint32_t bQFull = bar(0);
@@ -253,20 +273,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t once = l2_policy_evict_first();
       const int zq = b * p.Hq + hq;
       const int zk = b * p.Hkv + hk;
-      mbar_arrive_expect_tx(bQFull, C::kTileBytes * (has_b ? 2 : 1));
+      mbar_arrive_expect_tx(bQFull, C::kQKTileBytes * (has_b ? 2 : 1));
       for (int x = 0; x < (has_b ? 2 : 1); ++x)
-        for (int c = 0; c < C::kBoxes; ++c)
-          tma_load_3d(sQ + x * C::kTileBytes + c * kBoxBytes, &tmQ, bQFull,
-                      c * kBoxCols, row0[x], zq, once);
+        for (int c = 0; c < C::kQKBoxes; ++c)
+          tma_load_3d(sQ + x * C::kQKTileBytes + c * kBoxBytes, &tmQ, bQFull,
+                      c * C::kQKBoxCols, row0[x], zq, once);
       int k_issued = 0, v_issued = 0;
       for (int i = 0; i < n_blocks; ++i) {
         const int j = j0 + i;                    // block index in the pair
         const int sk = i % NK, sv = i % NV;
         if (!mbar_wait(bKEmpty(sk), ((i / NK) & 1) ^ 1, wc)) break;
-        mbar_arrive_expect_tx(bKFull(sk), C::kTileBytes);
-        for (int c = 0; c < C::kBoxes; ++c)
-          tma_load_3d(sK + sk * C::kTileBytes + c * kBoxBytes, &tmK,
-                      bKFull(sk), c * kBoxCols, j * kBN, zk, keep);
+        mbar_arrive_expect_tx(bKFull(sk), C::kQKTileBytes);
+        for (int c = 0; c < C::kQKBoxes; ++c)
+          tma_load_3d(sK + sk * C::kQKTileBytes + c * kBoxBytes, &tmK,
+                      bKFull(sk), c * C::kQKBoxCols, j * kBN, zk, keep);
         k_issued = i + 1;
         if (!mbar_wait(bVEmpty(sv), ((i / NV) & 1) ^ 1, wc)) break;
         mbar_arrive_expect_tx(bVFull(sv), C::kTileBytes);
@@ -294,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dK = sdesc_sw128(sK, 16, 1024);
     const uint64_t dV = sdesc_sw128(sV, kBoxBytes, 1024);
     constexpr uint64_t kStep = static_cast<uint64_t>(C::kTileBytes >> 4);
+    constexpr uint64_t kQKStep = static_cast<uint64_t>(C::kQKTileBytes >> 4);
     bool ok = __all_sync(kAll, mbar_wait(bQFull, 0, wc));
     // j counts this CTA's blocks (ring position); block j0 + j of the pair
     for (int j = 0; ok && j <= n_blocks; ++j) {
@@ -306,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j < n_blocks &&
           !(ok = __all_sync(kAll, mbar_wait(bKFull(s), (j / NK) & 1, wc))))
         break;
-      const uint64_t dKs = dK + static_cast<uint64_t>(s) * kStep;
+      const uint64_t dKs = dK + static_cast<uint64_t>(s) * kQKStep;
       const uint64_t dVs = dV + static_cast<uint64_t>(sp) * kStep;
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
@@ -321,9 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // S_x(j) = Q_x K_j^T
         if (j < n_blocks && j0 + j < nblk[x]) {
-          issue_qk<D>(tmem + C::col_s(x),
-                      dQ + static_cast<uint64_t>(x) * kStep, dKs,
-                      C::kIdescS);
+          issue_qk<D, QK8>(tmem + C::col_s(x),
+                           dQ + static_cast<uint64_t>(x) * kQKStep, dKs,
+                           C::kIdescS);
           mma_commit_w(bSFull(x));
         }
       }

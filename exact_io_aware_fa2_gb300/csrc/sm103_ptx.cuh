@@ -207,6 +207,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn,
          ((static_cast<uint32_t>(M) >> 4) << 24);
 }
 
+// Instruction descriptor of tcgen05.mma.kind::f8f6f4 with e4m3 A and B
+// (format code 0 in bits 7-9 and 10-12), fp32 accumulation (bits 4-5 = 1),
+// both operands K-major; N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | ((static_cast<uint32_t>(N) >> 3) << 17) |
+         ((static_cast<uint32_t>(M) >> 4) << 24);
+}
+
 // Warp-wide forms: every lane of a converged warp executes the call with the
 // same operands and one lane, chosen by elect.sync, issues the instruction.
 // Keeping the issuing code warp-uniform lets the compiler hold descriptors
@@ -223,6 +231,19 @@ __device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc,
       "setp.ne.b32 p, %4, 0;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
           d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T with 8-bit A and B (kind::f8f6f4).
+template <int ACC>
+__device__ __forceinline__ void mma_ss8_w(uint32_t d_tmem, uint64_t a_desc,
+                                          uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::
+          "r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(ACC)
       : "memory");
 }

@@ -28,6 +28,7 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_VALUE", 2: "FA_ERR_UNSUPPORTED",
                 3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
 # Every symbol the header declares.
 SYMBOLS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_noalloc",
+           "fa_fwd_qk8",
            "fa_status_string", "fa_last_device_error",
            "fa_probe_bounded_wait", "fa_version")
 
@@ -69,6 +70,10 @@ def load():
         lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci,
                                        ci, ctypes.c_float, ci, vp]
         lib.fa_fwd_noalloc.restype = ci
+        lib.fa_fwd_qk8.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci,
+                                   ctypes.c_float, ctypes.c_float,
+                                   ctypes.c_float, ci, vp]
+        lib.fa_fwd_qk8.restype = ci
         lib.fa_status_string.argtypes = [ci]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_last_device_error.argtypes = []
@@ -192,6 +197,54 @@ def fwd(q, k, v, scale=None, causal=False, out=None, lse=None,
                         lse.data_ptr() if lse is not None else 0,
                         B, Hq, Hkv, Nq, Nkv, D, scale, causal,
                         workspace.data_ptr() if need > 0 else 0, need, stream)
+    if st != FA_OK:
+        raise FAError(st)
+    return out, lse
+
+
+def fwd_qk8_raw(q8_ptr, k8_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, Nq, Nkv,
+                D, scale, q_descale, k_descale, causal, stream_handle):
+    """Direct call of ``fa_fwd_qk8``; returns the status."""
+    return int(load().fa_fwd_qk8(
+        ctypes.c_void_p(q8_ptr), ctypes.c_void_p(k8_ptr),
+        ctypes.c_void_p(v_ptr), ctypes.c_void_p(o_ptr),
+        ctypes.c_void_p(lse_ptr), B, Hq, Hkv, Nq, Nkv, D,
+        ctypes.c_float(scale), ctypes.c_float(q_descale),
+        ctypes.c_float(k_descale), 1 if causal else 0,
+        ctypes.c_void_p(stream_handle)))
+
+
+def fwd_qk8(q8, k8, v, scale=None, q_descale=1.0, k_descale=1.0,
+            causal=False, out=None, lse=None):
+    """Forward with e4m3 Q and K (``torch.float8_e4m3fn``, with one descale
+    factor each) and bf16 V, through ``fa_fwd_qk8``; D must be 128."""
+    for name, t, dt in (("q8", q8, torch.float8_e4m3fn),
+                        ("k8", k8, torch.float8_e4m3fn),
+                        ("v", v, torch.bfloat16)):
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [B, H, N, D]")
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.device != q8.device or t.device.type != "cuda":
+            raise ValueError("q8, k8, v must be CUDA tensors on one device")
+    B, Hq, Nq, D = q8.shape
+    if k8.shape != v.shape or k8.shape[0] != B or k8.shape[3] != D:
+        raise ValueError("k8, v must be [B, Hkv, Nkv, D] matching q8")
+    Hkv, Nkv = k8.shape[1], k8.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dev = q8.device
+    if out is None:
+        out = torch.empty(B, Hq, Nq, D, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = fwd_qk8_raw(q8.data_ptr(), k8.data_ptr(), v.data_ptr(),
+                         out.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Nq, Nkv,
+                         D, scale, q_descale, k_descale, causal,
+                         torch.cuda.current_stream(dev).cuda_stream)
     if st != FA_OK:
         raise FAError(st)
     return out, lse

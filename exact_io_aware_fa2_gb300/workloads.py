@@ -40,6 +40,8 @@ class Workload:
     q_std: float = 1.0
     k_spike_frac: float = 0.0
     k_spike_mult: float = 1.0
+    # Q and K quantised per tensor to e4m3 (the fa_fwd_qk8 path)
+    qk8: bool = False
 
     @property
     def scale(self):
@@ -85,6 +87,9 @@ WORKLOADS = {
         # one-tile kernel.
         Workload("splitkv_b1_hq32_hkv8_q128_kv32768_d256", 1, 32, 8, 128,
                  32768, 256, False),
+        # The pages' shape with e4m3 Q and K (per-tensor descales).
+        Workload("qk8_b1_h8_q4096_kv8192_d128", 1, 8, 8, 4096, 8192, 128,
+                 False, qk8=True),
     ]
 }
 
@@ -133,3 +138,24 @@ def make_custom_on_device(B, Hq, Hkv, Nq, Nkv, D, seed=0, device="cuda"):
         out.append(torch.randn(shape, generator=gen, device=device,
                                dtype=torch.bfloat16))
     return tuple(out)
+
+
+E4M3_MAX = 448.0
+
+
+def quantize_e4m3(t):
+    """Per-tensor e4m3 quantisation of a bf16 tensor: descale = amax / 448,
+    values t / descale rounded to e4m3.  Returns (t8, descale)."""
+    amax = float(t.float().abs().max())
+    descale = amax / E4M3_MAX if amax > 0 else 1.0
+    return (t.float() / descale).to(torch.float8_e4m3fn), descale
+
+
+def make_qk8_inputs(B, Hq, Hkv, Nq, Nkv, D, seed=0, q_std=1.0):
+    """Seeded inputs of the e4m3 Q/K path: the N(0,1) bf16 Q, K, V of
+    make_custom with Q and K quantised per tensor.  Returns
+    (q8, k8, v, q_descale, k_descale)."""
+    q, k, v = make_custom(B, Hq, Hkv, Nq, Nkv, D, seed=seed, q_std=q_std)
+    q8, qd = quantize_e4m3(q)
+    k8, kd = quantize_e4m3(k)
+    return q8, k8, v, qd, kd

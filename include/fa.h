@@ -116,6 +116,32 @@ int fa_fwd_ws(const void* q, const void* k, const void* v, void* o,
 int fa_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
                           int causal, size_t* bytes);
 
+/*
+ * fa_fwd_qk8 — fa_fwd with Q and K in 8-bit floating point (e4m3).
+ *
+ * The low-precision MMA path that "Flash Attention на 5090 в CUDA C++" sets
+ * as its goal (introduction; "Что дальше": MXFP8/NVFP4 MMA), in its plainest
+ * form: S = Q K^T runs on the tensor cores as an e4m3 x e4m3 product with
+ * fp32 accumulation (tcgen05 kind::f8f6f4), with one descale factor per
+ * tensor; P V stays bf16.  Block-scaled formats are not supported.
+ *
+ *   q8   device pointer, e4m3 (1 byte) [B, Hq,  Nq,  D], contiguous
+ *   k8   device pointer, e4m3 (1 byte) [B, Hkv, Nkv, D], contiguous
+ *   v, o, lse, B, Hq, Hkv, Nq, Nkv, causal, stream: as for fa_fwd
+ *   D    must be 128 (FA_ERR_UNSUPPORTED otherwise)
+ *   scale, q_descale, k_descale   the scores are
+ *        scale * q_descale * k_descale * (q8 . k8), with q8 and k8 taken
+ *        exactly as e4m3 values; the descales must be finite and > 0
+ *        (FA_ERR_INVALID_VALUE otherwise)
+ *
+ * Ownership, validation, asynchrony, split-KV scratch and error behaviour
+ * are those of fa_fwd.
+ */
+int fa_fwd_qk8(const void* q8, const void* k8, const void* v, void* o,
+               float* lse, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+               float scale, float q_descale, float k_descale, int causal,
+               void* stream);
+
 /* Size of the fixed scratch array behind fa_fwd_noalloc (32 MiB). */
 #define FA_NOALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -150,7 +150,9 @@ def _sample_rows(Nq, gen, extra=16):
     return sorted(r for r in fixed.union(rnd) if 0 <= r < Nq)
 
 
-@pytest.mark.parametrize("name", [n for n in WORKLOADS if n != "tiny_128_d64"])
+@pytest.mark.parametrize("name", [n for n in WORKLOADS
+                                  if n != "tiny_128_d64"
+                                  and not WORKLOADS[n].qk8])
 def test_workload_full_size_sampled(name):
     w = WORKLOADS[name]
     q, k, v = make_inputs(w)
