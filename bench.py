@@ -110,9 +110,10 @@ KERNEL_SOURCES = {
 
 
 def kernel_for(w):
-    """The kernel that runs a workload (head dims 192 and 256 take the
-    one-tile kernel)."""
-    return "fa_fwd_wide_kernel" if w.D in (192, 256) else "fa_fwd_kernel"
+    """The kernel that runs a workload (head dims 192 and 256, and causal
+    shapes at head dim 64, take the one-tile kernel)."""
+    one_tile = w.D in (192, 256) or (w.D == 64 and w.causal)
+    return "fa_fwd_wide_kernel" if one_tile else "fa_fwd_kernel"
 
 
 def kernel_source_hash(kernel="fa_fwd_kernel"):

@@ -77,7 +77,13 @@ cudaError_t opt_in_smem_wide() {
 bool supported_head_dim(int D) {
   return D == 64 || D == 128 || D == 192 || D == 256;
 }
-bool wide_head_dim(int D) { return D == 192 || D == 256; }
+// Shapes that run the one-tile kernel (fa_fwd_wide.cuh): head dims 192 and
+// 256 always; head dim 64 when causal, where many short CTAs gain from two
+// sharing an SM (measured: causal B4 H16 N2048 503 vs 463 TFLOPS, while the
+// non-causal 4096x8192 shape runs 796 on the two-tile kernel vs 765).
+bool one_tile(int D, int causal) {
+  return D == 192 || D == 256 || (D == 64 && causal);
+}
 
 int* g_status_word[kMaxDevices];
 int g_sm_count[kMaxDevices];
@@ -112,6 +118,8 @@ int device_ready(int** word_out, int* dev_out = nullptr) {
         opt_in_smem<128, true>() != cudaSuccess ||
         opt_in_smem<128, false, true>() != cudaSuccess ||
         opt_in_smem<128, true, true>() != cudaSuccess ||
+        opt_in_smem_wide<64, false>() != cudaSuccess ||
+        opt_in_smem_wide<64, true>() != cudaSuccess ||
         opt_in_smem_wide<192, false>() != cudaSuccess ||
         opt_in_smem_wide<192, true>() != cudaSuccess ||
         opt_in_smem_wide<256, false>() != cudaSuccess ||
@@ -159,13 +167,15 @@ constexpr int kSplitOverheadBlocks = 3;
 
 // Query rows per CTA and keys per K/V block of the kernel a head dim runs
 // (the two-tile kernel: 256 and 128; the wide-head kernel: 128 and 64).
-int unit_rows(int D) {
-  return wide_head_dim(D) ? fa::kBM : fa::kBM * fa::kTilesPerCta;
+int unit_rows(int D, int causal) {
+  return one_tile(D, causal) ? fa::kBM : fa::kBM * fa::kTilesPerCta;
 }
-int block_keys(int D) { return wide_head_dim(D) ? 64 : fa::kBN; }
+int block_keys(int D, int causal) {
+  return one_tile(D, causal) ? 64 : fa::kBN;
+}
 
 int plan_splits(int B, int Hq, int Nq, int Nkv, int D, int causal, int sms) {
-  const int rows_u = unit_rows(D), keys_b = block_keys(D);
+  const int rows_u = unit_rows(D, causal), keys_b = block_keys(D, causal);
   const long long units = (Nq + rows_u - 1) / rows_u;
   const long long ctas = units * Hq * B;
   if (ctas * 2 > sms) return 1;
@@ -208,9 +218,10 @@ RunShape run_shape(int Hq, int Hkv, int Nq, int causal) {
 
 // Split-KV scratch: one fp32 slot of unit_rows(D) * (D + 2) words per
 // (batch, head, unit of query rows, K/V range).
-int64_t workspace_bytes(int B, int Hq, int Nq, int D, int splits) {
+int64_t workspace_bytes(int B, int Hq, int Nq, int D, int causal,
+                        int splits) {
   if (splits <= 1) return 0;
-  const int64_t rows_u = unit_rows(D);
+  const int64_t rows_u = unit_rows(D, causal);
   const int64_t units = (Nq + rows_u - 1) / rows_u;
   const int64_t slot = rows_u * (D + 2);
   return static_cast<int64_t>(B) * Hq * units * splits * slot * 4;
@@ -385,7 +396,7 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
   p.wait_limit_ns = kWaitLimitNs;
   p.kv_splits = plan_splits(B, Hq, Nq, Nkv, D, causal, g_sm_count[dev]);
   p.work = nullptr;
-  const int64_t need = workspace_bytes(B, Hq, Nq, D, p.kv_splits);
+  const int64_t need = workspace_bytes(B, Hq, Nq, D, causal, p.kv_splits);
   void* owned = nullptr;
   if (need > 0) {
     if (pool_scratch) {
@@ -402,9 +413,7 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
   }
 
   CUtensorMap tq, tk, tv;
-  const int kv_rows = !wide_head_dim(D) ? fa::kBN
-                      : D == 192          ? fa::WideCfg<192>::kBN
-                                          : fa::WideCfg<256>::kBN;
+  const int kv_rows = one_tile(D, causal) ? fa::WideCfg<256>::kBN : fa::kBN;
   const bool qk_ok =
       qk8 ? (encode_bhnd_e4m3(&tq, q, static_cast<long long>(B) * Hq, Nq,
                               D) == FA_OK &&
@@ -429,6 +438,9 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
   else if (D == 192)
     st = causal ? launch_wide<192, true>(tq, tk, tv, p, B, Hq, Nq, s)
                 : launch_wide<192, false>(tq, tk, tv, p, B, Hq, Nq, s);
+  else if (D == 64 && one_tile(D, causal))
+    st = causal ? launch_wide<64, true>(tq, tk, tv, p, B, Hq, Nq, s)
+                : launch_wide<64, false>(tq, tk, tv, p, B, Hq, Nq, s);
   else if (D == 64)
     st = causal ? launch<64, true>(tq, tk, tv, p, B, Hq, Nq, s)
                 : launch<64, false>(tq, tk, tv, p, B, Hq, Nq, s);
@@ -483,7 +495,7 @@ int fa_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
   if (st != FA_OK) return st;
   const RunShape rs = run_shape(Hq, Hkv, Nq, causal);
   *bytes = static_cast<size_t>(workspace_bytes(
-      B, rs.Hq, rs.Nq, D,
+      B, rs.Hq, rs.Nq, D, causal,
       plan_splits(B, rs.Hq, rs.Nq, Nkv, D, causal, g_sm_count[dev])));
   return FA_OK;
 }

@@ -1,4 +1,5 @@
-// fa_fwd_wide.cuh — the attention forward for head dims 192 and 256.
+// fa_fwd_wide.cuh — the attention forward with one query tile per CTA: head
+// dims 192 and 256, and causal shapes at head dim 64 (two CTAs per SM).
 //
 // Same method as fa_fwd_kernel.cuh ("Hacker News Digest — gpu-computing",
 // section "Алгоритм Flash Attention 2", with the online softmax of section
@@ -26,6 +27,11 @@
 // pv_done barrier.  The wait is unambiguous: PV(j+1) cannot run before this
 // softmax publishes P(j+1).
 //
+// At head dim 64 the CTA needs 192 TMEM columns (256 allocated) and about
+// 64 KiB of shared memory, so two CTAs share an SM: they keep its tensor
+// pipe busy in turn, and one's start-up and epilogue overlap the other's
+// work, which pays for causal shapes with many short CTAs.
+//
 // Warp roles (192 threads): warp 0 MMA issuer (one elected lane), warp 1
 // TMA producer, warps 2-5 softmax (warp w owns rows 32*(w%4) .. +31 of the
 // tile, one row per thread).
@@ -42,7 +48,7 @@ constexpr int kWideSoftmaxWarp0 = 2;
 
 template <int D>
 struct WideCfg {
-  static_assert(D == 192 || D == 256, "wide head dim");
+  static_assert(D == 64 || D == 192 || D == 256, "one-tile head dim");
   // keys per K/V block: TMEM holds two S buffers of kBN columns and O
   static constexpr int kBN = 64;
   static constexpr int kBoxes = D / kBoxCols;              // 64-column boxes
@@ -58,9 +64,15 @@ struct WideCfg {
   // O final, drain
   static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 3;
   static constexpr int kBarBytes = 8 * kNumBars + 32;  // + tmem slot, waits
-  static constexpr int kSmemBytes = 1024 + kQBytes +
-                                    (kKStages + kVStages) * kKVBytes +
-                                    kBarBytes;
+  // At D = 64 two CTAs share an SM (TMEM: 2 x 64 S + 64 O columns, 256
+  // allocated): padding shared memory past a third of the SM's keeps a
+  // third CTA, which would wait for TMEM, from being scheduled beside them.
+  static constexpr int kCtasPerSm = (D == 64) ? 2 : 1;
+  static constexpr uint32_t kTmemAlloc = (D == 64) ? 256u : 512u;
+  static constexpr int kSmemUsed = 1024 + kQBytes +
+                                   (kKStages + kVStages) * kKVBytes + kBarBytes;
+  static constexpr int kSmemBytes =
+      (D == 64 && kSmemUsed < 80 * 1024) ? 80 * 1024 : kSmemUsed;
   static constexpr uint32_t kColO = 2 * kBN;
   // fp32 words of one split-KV partial slot: O rows [128][D] (unnormalised,
   // relative to the slot's reference max), then m[128], then l[128].
@@ -107,7 +119,7 @@ __device__ __forceinline__ void wide_issue_pv(uint32_t d_tmem, uint32_t a_tmem,
 // then processes that range of its tile's blocks and leaves fp32 partials
 // for fa_merge_kernel<D, 128>.
 template <int D, bool CAUSAL, bool SPLIT>
-__global__ void __launch_bounds__(kWideThreads, 1)
+__global__ void __launch_bounds__(kWideThreads, WideCfg<D>::kCtasPerSm)
     fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
@@ -186,7 +198,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     mbar_init_fence();
   }
   if (warp == kWideMmaWarp) {
-    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_alloc(smem_addr(tmem_slot), W::kTmemAlloc);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -488,7 +500,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kWideMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kWideMmaWarp) tmem_dealloc(tmem, W::kTmemAlloc);
 }
 
 }  // namespace fa

@@ -87,6 +87,8 @@ WORKLOADS = {
         # one-tile kernel.
         Workload("splitkv_b1_hq32_hkv8_q128_kv32768_d256", 1, 32, 8, 128,
                  32768, 256, False),
+        # The pages' shape at head dim 64.
+        Workload("d64_b1_h8_q4096_kv8192", 1, 8, 8, 4096, 8192, 64, False),
         # The pages' shape with e4m3 Q and K (per-tensor descales).
         Workload("qk8_b1_h8_q4096_kv8192_d128", 1, 8, 8, 4096, 8192, 128,
                  False, qk8=True),

@@ -62,7 +62,8 @@ typedef enum {
  *   lse  device pointer, fp32 [B, Hq,  Nq], contiguous; written; may be NULL
  *   B, Hq, Hkv, Nq, Nkv, D   sizes; Hq must be a multiple of Hkv (query head
  *        h reads kv head h / (Hq / Hkv)); D in {64, 128, 192, 256}
- *        (192 and 256 run a kernel with one 128-row query tile per CTA)
+ *        (192 and 256, and causal shapes at 64, run a kernel with one
+ *        128-row query tile per CTA)
  *   scale  finite fp32 multiplier of Q K^T (typically 1/sqrt(D))
  *   causal 0: every key visible; nonzero: key j visible to query i iff j <= i
  *   stream a cudaStream_t (as void*); NULL means the legacy default stream
