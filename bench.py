@@ -91,6 +91,24 @@ def job_tflops(flops_per_rank, ms_slowest, world_size):
     return world_size * flops_per_rank / (ms_slowest * 1e-3) / 1e12
 
 
+def hbm_peak():
+    """Measured copy bandwidth (GB/s) from MEASURED_PEAKS.json, or None."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f).get("hbm_gbs", 0.0)) or None
+    return None
+
+
+# The pages' own figures, on other hardware: context, not targets.
+PAGES_CONTEXT = {
+    "rtx5090_tflops_b1_h8_q4096_kv8192_bf16": [186.7, 203.6],
+    "rtx5090_sol_tflops": 209.5,
+    "thunderkittens_h100_tensor_util_claimed": 0.95,
+    "note": "figures the pages print for other GPUs (RTX 5090, H100)",
+}
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -402,6 +420,10 @@ def run_ours(args, w):
     value = job_tflops(w.flops, ms_max, ws)
     per_launch_tflops = w.flops / (ms * 1e-3) / 1e12
     peak, peak_src = peaks()
+    # DRAM bytes of one launch (ncu, committed) over its measured time
+    traffic = recorded_traffic(w)
+    hbm_gbs = traffic / (ms * 1e-3) / 1e9 if traffic else None
+    hbm_frac = (hbm_gbs / hbm_peak()) if hbm_gbs and hbm_peak() else None
     peak_src += ", of measured" if "MEASURED" in peak_src else ", of fallback"
     if w.qk8:
         # Half the flops (Q K^T) run as e4m3 products at twice the bf16 rate
@@ -482,11 +504,14 @@ def run_ours(args, w):
                      "peak": peak, "unit": "TFLOP/s",
                      "frac": per_launch_tflops / peak,
                      "peak_source": peak_src,
-                     "traffic": recorded_traffic(w),
+                     "traffic": traffic,
+                     "hbm_gbs_achieved": hbm_gbs,
+                     "hbm_frac_of_measured_copy": hbm_frac,
                      "kernel": "fa_fwd_kernel<SPLIT> + fa_merge_kernel"
                      if split else kernel_for(w),
                      "algorithmic_flops_per_launch": w.flops},
         "cpu_baseline": cpu,
+        "pages_context": PAGES_CONTEXT if w.name == HEADLINE else None,
         "e2e": {"value": job_tflops(w.flops, e2e_s * 1e3, ws), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s * 1e3},
