@@ -277,8 +277,22 @@ int launch_merge(const fa::FwdParams& p, int B, int Hq, int Nq,
                  cudaStream_t stream) {
   using M = fa::MergeCfg<D>;
   const int units = (Nq + ROWS - 1) / ROWS;
-  dim3 mgrid(units * (ROWS / M::kRowsPerBlock), Hq, B);
-  fa::fa_merge_kernel<D, ROWS><<<mgrid, M::kThreads, 0, stream>>>(p);
+  // Programmatic serialization: the merge grid is scheduled once every
+  // forward CTA has reached its epilogue, and waits (griddepcontrol.wait)
+  // for the forward grid to complete before reading the partials.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(units * (ROWS / M::kRowsPerBlock), Hq, B);
+  cfg.blockDim = dim3(M::kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, fa::fa_merge_kernel<D, ROWS>, p) !=
+      cudaSuccess)
+    return FA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

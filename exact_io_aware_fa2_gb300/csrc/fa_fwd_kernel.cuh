@@ -515,6 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- epilogue ----
+    // The merge of split-KV partials may be scheduled from here on; it
+    // waits for this whole grid before it reads them.
+    if constexpr (SPLIT) grid_dep_launch();
     if constexpr (SPLIT) {
       // Partial of one K/V range: unnormalised O (relative to m_ref), m and
       // l per row, for fa_merge_kernel.  A tile with no block in this range
@@ -624,6 +627,8 @@ __global__ void __launch_bounds__(MergeCfg<D>::kThreads)
   const int ch = static_cast<int>(threadIdx.x) % M::kChunks;
   const int hq = blockIdx.y, b = blockIdx.z;
   const int q_row = unit * ROWS + prow;
+  // Launched while the forward grid runs: wait for it (and its partials).
+  grid_dep_wait();
   if (q_row >= p.Nq) return;
   const int n_units = (p.Nq + ROWS - 1) / ROWS;
   const float* base = p.work + ((static_cast<int64_t>(b) * p.Hq + hq) *

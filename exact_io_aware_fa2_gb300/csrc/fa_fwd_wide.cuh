@@ -432,6 +432,9 @@ __global__ void __launch_bounds__(kWideThreads, WideCfg<D>::kCtasPerSm)
     }
 
     // ---- epilogue ----
+    // The merge of split-KV partials may be scheduled from here on; it
+    // waits for this whole grid before it reads them.
+    if constexpr (SPLIT) grid_dep_launch();
     if (ok && nblk > 0) ok = __all_sync(kAll, mbar_wait(bOFinal, 0, wc));
     const int trow = (warp & 3) * 32 + lane;         // row within the tile
     const uint32_t o_addr = tmem + lane_off + W::kColO;
