@@ -122,16 +122,24 @@ def peaks():
 # file leave recorded counters valid).
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ("fa_fwd_kernel.cuh", "sm103_ptx.cuh"),
+    "fa_fwd_stream_kernel": ("fa_fwd_stream.cuh", "fa_fwd_kernel.cuh",
+                             "sm103_ptx.cuh"),
     "fa_fwd_wide_kernel": ("fa_fwd_wide.cuh", "fa_fwd_kernel.cuh",
                            "sm103_ptx.cuh"),
 }
 
 
 def kernel_for(w):
-    """The kernel that runs a workload (head dims 192 and 256, and causal
-    shapes at head dim 64, take the one-tile kernel)."""
+    """The attention kernel that runs a workload on this device (head dims
+    192 and 256, and causal shapes at head dim 64, take the one-tile kernel;
+    the stream schedule has its own kernel)."""
     one_tile = w.D in (192, 256) or (w.D == 64 and w.causal)
-    return "fa_fwd_wide_kernel" if one_tile else "fa_fwd_kernel"
+    if one_tile:
+        return "fa_fwd_wide_kernel"
+    from exact_io_aware_fa2_gb300 import fa
+    sch = fa.schedule(w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D, w.causal)
+    return "fa_fwd_stream_kernel" if sch["kind"] == "stream" \
+        else "fa_fwd_kernel"
 
 
 def kernel_source_hash(kernel="fa_fwd_kernel"):
@@ -433,8 +441,8 @@ def run_ours(args, w):
         peak_src += "; x4/3: QK^T at the e4m3 rate (2x bf16), PV at bf16"
     # A split-KV step is the forward kernel plus the merge; the step time
     # (both kernels) then stands for the forward kernel's, a lower bound.
-    split = fa.workspace_size(w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D,
-                              w.causal) > 0
+    sched = fa.schedule(w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D, w.causal)
+    split = sched["kind"] == "split_kv"
     launches_per_step = 2 if split else 1
 
     # ---- end to end through the public API with host buffers ----
@@ -507,8 +515,9 @@ def run_ours(args, w):
                      "traffic": traffic,
                      "hbm_gbs_achieved": hbm_gbs,
                      "hbm_frac_of_measured_copy": hbm_frac,
-                     "kernel": "fa_fwd_kernel<SPLIT> + fa_merge_kernel"
+                     "kernel": f"{kernel_for(w)}<SPLIT> + fa_merge_kernel"
                      if split else kernel_for(w),
+                     "schedule": sched,
                      "algorithmic_flops_per_launch": w.flops},
         "cpu_baseline": cpu,
         "pages_context": PAGES_CONTEXT if w.name == HEADLINE else None,

@@ -6,12 +6,15 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
 
 #include "fa.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_fwd_stream.cuh"
 #include "fa_fwd_wide.cuh"
 
 namespace fa {
@@ -59,6 +62,13 @@ cudaError_t opt_in_smem() {
   return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, true, QK8>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmem);
+}
+
+template <int D, bool QK8 = false>
+cudaError_t opt_in_smem_stream() {
+  return cudaFuncSetAttribute(fa::fa_fwd_stream_kernel<D, QK8>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              fa::StreamCfg<D, QK8>::kSmemBytes);
 }
 
 template <int D, bool CAUSAL>
@@ -118,6 +128,9 @@ int device_ready(int** word_out, int* dev_out = nullptr) {
         opt_in_smem<128, true>() != cudaSuccess ||
         opt_in_smem<128, false, true>() != cudaSuccess ||
         opt_in_smem<128, true, true>() != cudaSuccess ||
+        opt_in_smem_stream<64>() != cudaSuccess ||
+        opt_in_smem_stream<128>() != cudaSuccess ||
+        opt_in_smem_stream<128, true>() != cudaSuccess ||
         opt_in_smem_wide<64, false>() != cudaSuccess ||
         opt_in_smem_wide<64, true>() != cudaSuccess ||
         opt_in_smem_wide<192, false>() != cudaSuccess ||
@@ -200,6 +213,66 @@ int plan_splits(int B, int Hq, int Nq, int Nkv, int D, int causal, int sms) {
   return static_cast<int>(best_s);
 }
 
+// Stream schedule (fa_fwd_stream.cuh; two-tile kernel, no causal mask):
+// when whole tile pairs leave SMs idle in their last wave, give every CTA
+// an equal contiguous share of all (pair, K/V block) items instead.  Costs
+// in units of one K/V block of one pair on the two-tile kernel, fitted to
+// GB300 timings of both schedules (D = 128, 8192 keys; 80 to 256 pairs;
+// 2048 keys for short rows):
+//   plain  = waves x blocks per pair + kPairOverheadBlocks
+//   stream = kStreamBlockFactor x blocks per CTA + kStreamOverheadBlocks
+//            + kSegmentBlocks x (segments per CTA - 1)
+// (the stream kernel's blocks are 4% slower, and its partial writes, merges
+// and segment switches cost about 11 blocks more than the plain kernel's
+// start-up and epilogue).  Stream runs when estimated at least kStreamGain
+// faster and a CTA's share is at least half a pair (a merger then combines
+// at most two partials); measured 26% faster at 80 pairs, 18% at 200, and
+// 8% slower at 128 pairs (128 of 152 SMs busy), which the estimate leaves
+// to the plain kernel.
+constexpr double kPairOverheadBlocks = 7.0;
+constexpr double kStreamBlockFactor = 1.04;
+constexpr double kStreamOverheadBlocks = 18.0;
+constexpr double kSegmentBlocks = 2.5;
+constexpr double kStreamGain = 0.97;
+
+// Schedule forced by fa_set_schedule (FA_SCHEDULE_AUTO: the estimate).
+std::atomic<int> g_forced_schedule{FA_SCHEDULE_AUTO};
+
+struct Plan {
+  int splits;       // split-KV pieces per unit of query rows (1: none)
+  int stream_len;   // K/V blocks per CTA of the stream schedule (0: off)
+  int stream_ctas;  // CTAs of the stream schedule
+};
+
+Plan plan_forward(int B, int Hq, int Nq, int Nkv, int D, int causal,
+                  int sms) {
+  const int forced = g_forced_schedule.load(std::memory_order_relaxed);
+  if (forced == FA_SCHEDULE_PLAIN) return Plan{1, 0, 0};
+  const bool stream_ok = !causal && !one_tile(D, causal);
+  Plan pl{1, 0, 0};
+  if (forced != FA_SCHEDULE_STREAM || !stream_ok)
+    pl.splits = plan_splits(B, Hq, Nq, Nkv, D, causal, sms);
+  if (pl.splits > 1 || !stream_ok) return pl;
+  const int64_t pairs = static_cast<int64_t>(B) * Hq *
+                        ((Nq + 2 * fa::kBM - 1) / (2 * fa::kBM));
+  const int64_t nbp = (Nkv + fa::kBN - 1) / fa::kBN;
+  const int64_t total = pairs * nbp;
+  const int64_t L = (total + sms - 1) / sms;
+  if (forced != FA_SCHEDULE_STREAM) {
+    const int64_t waves = (pairs + sms - 1) / sms;
+    const double plain = static_cast<double>(waves * nbp) +
+                         kPairOverheadBlocks;
+    const int64_t segments = (L - 1 + nbp - 1) / nbp + 1;   // at most
+    const double stream = kStreamBlockFactor * static_cast<double>(L) +
+                          kStreamOverheadBlocks +
+                          kSegmentBlocks * static_cast<double>(segments - 1);
+    if (2 * L < nbp || stream > kStreamGain * plain) return pl;
+  }
+  pl.stream_len = static_cast<int>(L);
+  pl.stream_ctas = static_cast<int>((total + L - 1) / L);
+  return pl;
+}
+
 // The shape the kernel runs.  Without a causal mask every query row of a
 // GQA group reads the same K/V, and the group's heads are adjacent in the
 // [B, Hq, Nq, D] layout (as are their O rows and LSE entries), so the group
@@ -216,10 +289,15 @@ RunShape run_shape(int Hq, int Hkv, int Nq, int causal) {
   return {Hkv, static_cast<int>(packed)};
 }
 
-// Split-KV scratch: one fp32 slot of unit_rows(D) * (D + 2) words per
-// (batch, head, unit of query rows, K/V range).
+// Scratch: for split-KV one fp32 slot of unit_rows(D) * (D + 2) words per
+// (batch, head, unit of query rows, K/V range); for the stream schedule one
+// slot per CTA plus its flags.
 int64_t workspace_bytes(int B, int Hq, int Nq, int D, int causal,
-                        int splits) {
+                        const Plan& pl) {
+  if (pl.stream_len > 0)
+    return D == 64 ? fa::stream_workspace_bytes<64>(pl.stream_ctas)
+                   : fa::stream_workspace_bytes<128>(pl.stream_ctas);
+  const int splits = pl.splits;
   if (splits <= 1) return 0;
   const int64_t rows_u = unit_rows(D, causal);
   const int64_t units = (Nq + rows_u - 1) / rows_u;
@@ -303,6 +381,18 @@ int launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
   constexpr int kSmem = fa::FwdCfg<D, QK8>::kSmemBytes;
   const int rows_per_cta = fa::kBM * fa::kTilesPerCta;
   const int pairs = (Nq + rows_per_cta - 1) / rows_per_cta;
+  if constexpr (!CAUSAL) {
+    if (p.stream_len > 0) {
+      const int64_t total = static_cast<int64_t>(B) * Hq * pairs *
+                            ((p.Nkv + fa::kBN - 1) / fa::kBN);
+      const dim3 sgrid(static_cast<unsigned>(
+          (total + p.stream_len - 1) / p.stream_len));
+      fa::fa_fwd_stream_kernel<D, QK8>
+          <<<sgrid, fa::kThreads, fa::StreamCfg<D, QK8>::kSmemBytes,
+             stream>>>(q, k, v, p);
+      return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    }
+  }
   dim3 grid(pairs, Hq, B * p.kv_splits);
   if (p.kv_splits > 1)
     fa::fa_fwd_kernel<D, CAUSAL, true, QK8>
@@ -333,6 +423,20 @@ int launch_wide(const CUtensorMap& q, const CUtensorMap& k,
   if (p.kv_splits > 1)
     return launch_merge<D, fa::kBM>(p, B, Hq, Nq, stream);
   return FA_OK;
+}
+
+// Value under which one launch's stream-schedule CTAs publish their
+// partials: distinct for every call of the process, never 0 (the value a
+// merger leaves behind), and starting from a clock-derived 64-bit value so
+// that scratch memory left by other work is unlikely to hold it.
+uint64_t next_epoch() {
+  static std::atomic<uint64_t> counter{
+      static_cast<uint64_t>(
+          std::chrono::steady_clock::now().time_since_epoch().count()) *
+      0x9E3779B97F4A7C15ull};
+  uint64_t e = counter.fetch_add(1, std::memory_order_relaxed);
+  if (e == 0) e = counter.fetch_add(1, std::memory_order_relaxed);
+  return e;
 }
 
 bool aligned(const void* p, uintptr_t a) {
@@ -408,9 +512,13 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
       (qk8 ? static_cast<double>(q_descale) * k_descale : 1.0));
   p.status = word;
   p.wait_limit_ns = kWaitLimitNs;
-  p.kv_splits = plan_splits(B, Hq, Nq, Nkv, D, causal, g_sm_count[dev]);
+  const Plan pl = plan_forward(B, Hq, Nq, Nkv, D, causal, g_sm_count[dev]);
+  p.kv_splits = pl.splits;
   p.work = nullptr;
-  const int64_t need = workspace_bytes(B, Hq, Nq, D, causal, p.kv_splits);
+  p.B = B;
+  p.stream_len = pl.stream_len;
+  p.epoch = next_epoch();
+  const int64_t need = workspace_bytes(B, Hq, Nq, D, causal, pl);
   void* owned = nullptr;
   if (need > 0) {
     if (pool_scratch) {
@@ -510,7 +618,44 @@ int fa_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
   const RunShape rs = run_shape(Hq, Hkv, Nq, causal);
   *bytes = static_cast<size_t>(workspace_bytes(
       B, rs.Hq, rs.Nq, D, causal,
-      plan_splits(B, rs.Hq, rs.Nq, Nkv, D, causal, g_sm_count[dev])));
+      plan_forward(B, rs.Hq, rs.Nq, Nkv, D, causal, g_sm_count[dev])));
+  return FA_OK;
+}
+
+int fa_set_schedule(int kind) {
+  if (kind != FA_SCHEDULE_AUTO && kind != FA_SCHEDULE_PLAIN &&
+      kind != FA_SCHEDULE_STREAM)
+    return FA_ERR_INVALID_VALUE;
+  g_forced_schedule.store(kind, std::memory_order_relaxed);
+  return FA_OK;
+}
+
+int fa_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                    int causal, int* kind, int* ctas, int* pieces,
+                    int* blocks_per_cta) {
+  if (kind == nullptr || ctas == nullptr || pieces == nullptr ||
+      blocks_per_cta == nullptr)
+    return FA_ERR_INVALID_VALUE;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nkv < 1 || D < 1 ||
+      Hq % Hkv != 0 || B > 65535 || Hq > 65535)
+    return FA_ERR_INVALID_VALUE;
+  if (!supported_head_dim(D)) return FA_ERR_UNSUPPORTED;
+  int dev = 0;
+  const int st = device_ready(nullptr, &dev);
+  if (st != FA_OK) return st;
+  const RunShape rs = run_shape(Hq, Hkv, Nq, causal);
+  const Plan pl =
+      plan_forward(B, rs.Hq, rs.Nq, Nkv, D, causal, g_sm_count[dev]);
+  const int64_t rows_u = unit_rows(D, causal);
+  const int64_t units = (rs.Nq + rows_u - 1) / rows_u;
+  *kind = pl.stream_len > 0 ? FA_SCHEDULE_STREAM
+          : pl.splits > 1   ? FA_SCHEDULE_SPLIT_KV
+                            : FA_SCHEDULE_PLAIN;
+  *ctas = pl.stream_len > 0
+              ? pl.stream_ctas
+              : static_cast<int>(units * rs.Hq * B * pl.splits);
+  *pieces = pl.splits;
+  *blocks_per_cta = pl.stream_len;
   return FA_OK;
 }
 

@@ -121,6 +121,11 @@ struct FwdParams {
   // fp32 partials in `work` (see kSlotFloats) for fa_merge_kernel.
   int kv_splits;
   float* work;
+  // Stream schedule (fa_fwd_stream.cuh): batch count, K/V blocks per CTA,
+  // and the value this launch's CTAs publish their partials under.
+  int B;
+  int stream_len;
+  uint64_t epoch;
 };
 
 // S = Q K^T for one tile and one K/V block: D/16 MMAs of 128x128x16.  Both
@@ -170,6 +175,190 @@ template <bool CAUSAL>
 __device__ __forceinline__ int kv_blocks(int row0, int Nkv) {
   const int end = CAUSAL ? min(Nkv, row0 + kBM) : Nkv;
   return (end + kBN - 1) / kBN;
+}
+
+// One K/V block of the online softmax, for the query row this thread owns
+// (TMEM lane = row): reads the block's scores from TMEM at s_addr, takes the
+// row's extreme over the visible keys, moves the reference max m_ref (log2
+// domain) only when the block exceeds it by more than kRescaleLog2, writes
+// P = exp2(s * c - m_ref) as packed bf16 to p_addr, adds the row sum to
+// l_run, and rescales O (at o_addr) when the reference moved and O already
+// holds earlier blocks (`o_live`).  Returns once its TMEM stores are done and
+// fenced; the caller then signals that P is ready.  Keys from col0 on are
+// visible up to Nkv and, when CAUSAL, up to the row's own index q_abs.
+// Steps: "Hacker News Digest — gpu-computing", section "v1 — базовая
+// версия", item 3 (running max and denominator); the lazy rescale is the
+// one-pass form of the same recurrence with a stale reference.
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void softmax_block(
+    uint32_t s_addr, uint32_t p_addr, uint32_t o_addr, int col0, int my_row0,
+    int q_abs, int Nkv, float c, bool neg_scale, bool o_live, float& m_ref,
+    float& l_run) {
+  uint32_t sr[kBN];
+  const bool need_mask =
+      (col0 + kBN > Nkv) || (CAUSAL && col0 + kBN - 1 > my_row0);
+  // Unmasked blocks take the row's extreme from reducing TMEM loads (one
+  // max/min per 32 columns, computed by the load itself).
+  float red[kBN / 32];
+  if (!need_mask && !neg_scale) {
+#pragma unroll
+    for (int cc = 0; cc < kBN / 32; ++cc)
+      tmem_ld32_max(s_addr + cc * 32, sr + cc * 32, red[cc]);
+  } else if (!need_mask) {
+#pragma unroll
+    for (int cc = 0; cc < kBN / 32; ++cc)
+      tmem_ld32_min(s_addr + cc * 32, sr + cc * 32, red[cc]);
+  } else {
+#pragma unroll
+    for (int cc = 0; cc < kBN / 32; ++cc) {
+      tmem_ld32(s_addr + cc * 32, sr + cc * 32);
+      red[cc] = 0.f;
+    }
+  }
+  tmem_ld_wait();
+#pragma unroll
+  for (int cc = 0; cc < kBN / 32; ++cc) {
+    reg_fence32(sr + cc * 32);
+    reg_fence_f(red[cc]);
+  }
+#define S_(i) __uint_as_float(sr[(i)])
+
+  // ---- row extreme over the visible keys of this block ----
+  int n_vis = kBN;   // keys [col0, col0 + n_vis) are visible to this row
+  if (need_mask) {
+    int lim = Nkv - col0;
+    if (CAUSAL) lim = min(lim, q_abs - col0 + 1);
+    n_vis = max(0, min(kBN, lim));
+  }
+  float ext;
+  if (!need_mask) {
+    ext = neg_scale ? fminf(fminf(red[0], red[1]), fminf(red[2], red[3]))
+                    : fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  } else {
+    // four independent chains of three-input extremes over the visible
+    // keys (the others take the identity)
+    const float idn = neg_scale ? INFINITY : -INFINITY;
+    float e4[4] = {idn, idn, idn, idn};
+#pragma unroll
+    for (int i = 0; i < kBN; i += 2) {
+      const float v0 = (i < n_vis) ? S_(i) : idn;
+      const float v1 = (i + 1 < n_vis) ? S_(i + 1) : idn;
+      float& e = e4[(i >> 1) & 3];
+      e = neg_scale ? fmin3(e, v0, v1) : fmax3(e, v0, v1);
+    }
+    ext = neg_scale ? fminf(fminf(e4[0], e4[1]), fminf(e4[2], e4[3]))
+                    : fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]));
+  }
+  const float m_blk = (n_vis > 0) ? ext * c : -INFINITY;
+  // Move the reference max only when this block exceeds it by more than
+  // the threshold (always on the first visible block).
+  const bool move = m_blk > m_ref + kRescaleLog2 ||
+                    (m_ref == -INFINITY && m_blk != -INFINITY);
+  const float m_new = move ? m_blk : m_ref;
+  const float alpha =
+      (move && m_ref != -INFINITY) ? ex2_approx(m_ref - m_new) : 1.f;
+  const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+
+  // ---- P = exp2(s * c - m), row sum, pack to bf16 ----
+  uint32_t pp[kBN / 2];
+  float rsum;
+  if (!need_mask) {
+    // x = s*c - m on packed pairs (f32x2 FMA), exp2 on the MUFU, packed
+    // row sums, bf16x2 packing of P.
+    const uint64_t c2 = f2(c, c);
+    const uint64_t nm2 = f2(-m_use, -m_use);
+    uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < kBN; i += 2) {
+      float x0, x1;
+      f2_split(fma2(f2(S_(i), S_(i + 1)), c2, nm2), x0, x1);
+      const float e0 = ex2_approx(x0);
+      const float e1 = ex2_approx(x1);
+      acc[(i >> 1) & 3] = add2(acc[(i >> 1) & 3], f2(e0, e1));
+      pp[i / 2] = pack_bf16x2(e0, e1);
+    }
+    float s0, s1;
+    f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), s0, s1);
+    rsum = s0 + s1;
+  } else {
+    // the same packed loop; invisible keys get x = -inf, so p = 0
+    const uint64_t c2 = f2(c, c);
+    const uint64_t nm2 = f2(-m_use, -m_use);
+    uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < kBN; i += 2) {
+      float x0, x1;
+      f2_split(fma2(f2(S_(i), S_(i + 1)), c2, nm2), x0, x1);
+      x0 = (i < n_vis) ? x0 : -INFINITY;
+      x1 = (i + 1 < n_vis) ? x1 : -INFINITY;
+      const float e0 = ex2_approx(x0);
+      const float e1 = ex2_approx(x1);
+      acc[(i >> 1) & 3] = add2(acc[(i >> 1) & 3], f2(e0, e1));
+      pp[i / 2] = pack_bf16x2(e0, e1);
+    }
+    float s0, s1;
+    f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), s0, s1);
+    rsum = s0 + s1;
+  }
+#undef S_
+  l_run = l_run * alpha + rsum;
+  m_ref = m_new;
+
+  // ---- rescale O when the reference max moved.  S(j) complete means
+  // every earlier MMA of the issuing thread, including the P*V of the
+  // previous block, is complete, so O is stable here. ----
+  if (o_live && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+    for (int cc = 0; cc < D / 32; ++cc) {
+      uint32_t orr[32];
+      tmem_ld32(o_addr + cc * 32, orr);
+      tmem_ld_wait();
+      reg_fence32(orr);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+      tmem_st32(o_addr + cc * 32, orr);
+    }
+  }
+  tmem_st32(p_addr, pp);
+  tmem_st32(p_addr + 32, pp + 32);
+  tmem_st_wait();
+  tc_fence_before();
+}
+
+// The last step for one query row: O (unnormalised, in TMEM at o_addr,
+// relative to the reference max m_ref) divided by the row sum l_run, rounded
+// to bf16 and stored at orow; LSE = (m_ref + log2 l_run) ln 2 at lse_at
+// (skipped when null).  Rows past the end (`in_range` false) store nothing.
+template <int D>
+__device__ __forceinline__ void store_final_row(uint32_t o_addr, float m_ref,
+                                                float l_run,
+                                                __nv_bfloat16* orow,
+                                                float* lse_at, bool in_range) {
+  const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+#pragma unroll
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t orr[32];
+    tmem_ld32(o_addr + cc * 32, orr);
+    tmem_ld_wait();
+    reg_fence32(orr);
+    uint32_t packed[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      packed[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
+                              __uint_as_float(orr[2 * i + 1]) * inv_l);
+    if (in_range) {
+      uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1],
+                            packed[4 * i + 2], packed[4 * i + 3]);
+    }
+  }
+  if (in_range && lse_at != nullptr) {
+    const float lse2 = (l_run > 0.f) ? (m_ref + log2f(l_run)) : -INFINITY;
+    *lse_at = lse2 * 0.69314718055994530942f;
+  }
 }
 
 // SPLIT: the grid's z index also carries the K/V range (split-KV) and the
@@ -376,140 +565,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mbar_wait(bSFull(x), j & 1, wc))))
         break;
       tc_fence_after();
-      uint32_t sr[kBN];
-      const uint32_t s_addr = tmem + lane_off + C::col_s(x);
-      const int col0 = (j0 + j) * kBN;
-      const bool need_mask =
-          (col0 + kBN > p.Nkv) || (CAUSAL && col0 + kBN - 1 > my_row0);
-      // Unmasked blocks take the row's extreme from reducing TMEM loads (one
-      // max/min per 32 columns, computed by the load itself).
-      float red[kBN / 32];
-      if (!need_mask && !neg_scale) {
-#pragma unroll
-        for (int cc = 0; cc < kBN / 32; ++cc)
-          tmem_ld32_max(s_addr + cc * 32, sr + cc * 32, red[cc]);
-      } else if (!need_mask) {
-#pragma unroll
-        for (int cc = 0; cc < kBN / 32; ++cc)
-          tmem_ld32_min(s_addr + cc * 32, sr + cc * 32, red[cc]);
-      } else {
-#pragma unroll
-        for (int cc = 0; cc < kBN / 32; ++cc) {
-          tmem_ld32(s_addr + cc * 32, sr + cc * 32);
-          red[cc] = 0.f;
-        }
-      }
-      tmem_ld_wait();
-#pragma unroll
-      for (int cc = 0; cc < kBN / 32; ++cc) {
-        reg_fence32(sr + cc * 32);
-        reg_fence_f(red[cc]);
-      }
-#define S_(i) __uint_as_float(sr[(i)])
-
-      // ---- row extreme over the visible keys of this block ----
-      int n_vis = kBN;   // keys [col0, col0 + n_vis) are visible to this row
-      if (need_mask) {
-        int lim = p.Nkv - col0;
-        if (CAUSAL) lim = min(lim, q_abs - col0 + 1);
-        n_vis = max(0, min(kBN, lim));
-      }
-      float ext;
-      if (!need_mask) {
-        ext = neg_scale ? fminf(fminf(red[0], red[1]), fminf(red[2], red[3]))
-                        : fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-      } else {
-        // four independent chains of three-input extremes over the visible
-        // keys (the others take the identity)
-        const float idn = neg_scale ? INFINITY : -INFINITY;
-        float e4[4] = {idn, idn, idn, idn};
-#pragma unroll
-        for (int i = 0; i < kBN; i += 2) {
-          const float v0 = (i < n_vis) ? S_(i) : idn;
-          const float v1 = (i + 1 < n_vis) ? S_(i + 1) : idn;
-          float& e = e4[(i >> 1) & 3];
-          e = neg_scale ? fmin3(e, v0, v1) : fmax3(e, v0, v1);
-        }
-        ext = neg_scale ? fminf(fminf(e4[0], e4[1]), fminf(e4[2], e4[3]))
-                        : fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]));
-      }
-      const float m_blk = (n_vis > 0) ? ext * c : -INFINITY;
-      // Move the reference max only when this block exceeds it by more than
-      // the threshold (always on the first visible block).
-      const bool move = m_blk > m_ref + kRescaleLog2 ||
-                        (m_ref == -INFINITY && m_blk != -INFINITY);
-      const float m_new = move ? m_blk : m_ref;
-      const float alpha =
-          (move && m_ref != -INFINITY) ? ex2_approx(m_ref - m_new) : 1.f;
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-
-      // ---- P = exp2(s * c - m), row sum, pack to bf16 ----
-      uint32_t pp[kBN / 2];
-      float rsum;
-      if (!need_mask) {
-        // x = s*c - m on packed pairs (f32x2 FMA), exp2 on the MUFU, packed
-        // row sums, bf16x2 packing of P.
-        const uint64_t c2 = f2(c, c);
-        const uint64_t nm2 = f2(-m_use, -m_use);
-        uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int i = 0; i < kBN; i += 2) {
-          float x0, x1;
-          f2_split(fma2(f2(S_(i), S_(i + 1)), c2, nm2), x0, x1);
-          const float e0 = ex2_approx(x0);
-          const float e1 = ex2_approx(x1);
-          acc[(i >> 1) & 3] = add2(acc[(i >> 1) & 3], f2(e0, e1));
-          pp[i / 2] = pack_bf16x2(e0, e1);
-        }
-        float s0, s1;
-        f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), s0, s1);
-        rsum = s0 + s1;
-      } else {
-        // the same packed loop; invisible keys get x = -inf, so p = 0
-        const uint64_t c2 = f2(c, c);
-        const uint64_t nm2 = f2(-m_use, -m_use);
-        uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int i = 0; i < kBN; i += 2) {
-          float x0, x1;
-          f2_split(fma2(f2(S_(i), S_(i + 1)), c2, nm2), x0, x1);
-          x0 = (i < n_vis) ? x0 : -INFINITY;
-          x1 = (i + 1 < n_vis) ? x1 : -INFINITY;
-          const float e0 = ex2_approx(x0);
-          const float e1 = ex2_approx(x1);
-          acc[(i >> 1) & 3] = add2(acc[(i >> 1) & 3], f2(e0, e1));
-          pp[i / 2] = pack_bf16x2(e0, e1);
-        }
-        float s0, s1;
-        f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), s0, s1);
-        rsum = s0 + s1;
-      }
-#undef S_
-      l_run = l_run * alpha + rsum;
-      m_ref = m_new;
-
-      // ---- rescale O when the reference max moved.  S_x(j) complete means
-      // every earlier MMA of this thread, including PV_x(j-1), is complete,
-      // so O_x is stable here. ----
-      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        const uint32_t o_addr = tmem + lane_off + C::col_o(x);
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t orr[32];
-          tmem_ld32(o_addr + cc * 32, orr);
-          tmem_ld_wait();
-          reg_fence32(orr);
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-          tmem_st32(o_addr + cc * 32, orr);
-        }
-      }
-      const uint32_t p_addr = tmem + lane_off + C::col_p(x);
-      tmem_st32(p_addr, pp);
-      tmem_st32(p_addr + 32, pp + 32);
-      tmem_st_wait();
-      tc_fence_before();
+      softmax_block<D, CAUSAL>(tmem + lane_off + C::col_s(x),
+                               tmem + lane_off + C::col_p(x),
+                               tmem + lane_off + C::col_o(x), (j0 + j) * kBN,
+                               my_row0, q_abs, p.Nkv, c, neg_scale, j >= 1,
+                               m_ref, l_run);
       __syncwarp();
       if (lane == 0) mbar_arrive(bPFull(x));
     }
@@ -555,36 +615,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bOFinal, 0, wc));
     if (ok && nb > 0) {
       tc_fence_after();
-      const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      const bool in_range = q_abs < p.Nq;
       const size_t row_idx =
           (static_cast<size_t>(b) * p.Hq + hq) * static_cast<size_t>(p.Nq) +
           static_cast<size_t>(q_abs);
-      __nv_bfloat16* orow = p.o + row_idx * D;
-      const uint32_t o_addr = tmem + lane_off + C::col_o(x);
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t orr[32];
-        tmem_ld32(o_addr + cc * 32, orr);
-        tmem_ld_wait();
-        reg_fence32(orr);
-        uint32_t packed[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          packed[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
-                                  __uint_as_float(orr[2 * i + 1]) * inv_l);
-        if (in_range) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1],
-                                packed[4 * i + 2], packed[4 * i + 3]);
-        }
-      }
-      if (in_range && p.lse != nullptr) {
-        const float lse2 = (l_run > 0.f) ? (m_ref + log2f(l_run)) : -INFINITY;
-        p.lse[row_idx] = lse2 * 0.69314718055994530942f;
-      }
+      store_final_row<D>(tmem + lane_off + C::col_o(x), m_ref, l_run,
+                         p.o + row_idx * D,
+                         p.lse != nullptr ? p.lse + row_idx : nullptr,
+                         q_abs < p.Nq);
     }
     }
   }

@@ -118,6 +118,44 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// ------------------------------------------------- flags between CTAs of a grid
+
+// Publish `v` at `flag` after every global store this thread made before
+// (release at GPU scope; callers fence and synchronise the warp first so the
+// other lanes' stores are included).
+__device__ __forceinline__ void flag_release(uint64_t* flag, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(flag), "l"(v)
+               : "memory");
+}
+__device__ __forceinline__ uint64_t flag_acquire(const uint64_t* flag) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(flag)
+               : "memory");
+  return v;
+}
+// Wait until *flag == v (acquire: this thread's later loads see what the
+// publisher stored before its release).  Same limit, abort flag and error
+// recording as mbar_wait.
+__device__ __forceinline__ bool flag_wait(const uint64_t* flag, uint64_t v,
+                                          const WaitCtx& w) {
+  if (flag_acquire(flag) == v) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(64);
+    if (flag_acquire(flag) == v) return true;
+    if (wait_aborted(w)) return false;
+    uint64_t limit;
+    asm volatile("ld.shared.u64 %0, [%1 + 16];" : "=l"(limit) : "r"(w.state));
+    if (globaltimer_ns() - t0 > limit) {
+      uint64_t status;
+      asm volatile("ld.shared.u64 %0, [%1 + 8];" : "=l"(status) : "r"(w.state));
+      atomicCAS(reinterpret_cast<int*>(status), 0, kStatusTimeout);
+      wait_raise_abort(w);
+      return false;
+    }
+  }
+}
+
 // --------------------------------------------- programmatic dependent launch
 
 // Let a grid launched after this one with programmatic serialization be

@@ -28,7 +28,7 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_VALUE", 2: "FA_ERR_UNSUPPORTED",
                 3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
 # Every symbol the header declares.
 SYMBOLS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_noalloc",
-           "fa_fwd_qk8",
+           "fa_fwd_qk8", "fa_fwd_schedule", "fa_set_schedule",
            "fa_status_string", "fa_last_device_error",
            "fa_probe_bounded_wait", "fa_version")
 
@@ -82,6 +82,12 @@ def load():
         lib.fa_probe_bounded_wait.restype = ci
         lib.fa_version.argtypes = []
         lib.fa_version.restype = ci
+        pi = ctypes.POINTER(ci)
+        lib.fa_fwd_schedule.argtypes = [ci, ci, ci, ci, ci, ci, ci, pi, pi,
+                                        pi, pi]
+        lib.fa_fwd_schedule.restype = ci
+        lib.fa_set_schedule.argtypes = [ci]
+        lib.fa_set_schedule.restype = ci
         _lib = lib
         return lib
 
@@ -140,6 +146,38 @@ def fwd_noalloc_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, Nq, Nkv,
         ctypes.c_void_p(o_ptr), ctypes.c_void_p(lse_ptr),
         B, Hq, Hkv, Nq, Nkv, D, ctypes.c_float(scale), 1 if causal else 0,
         ctypes.c_void_p(stream_handle)))
+
+
+# Schedule names of fa_fwd_schedule's FA_SCHEDULE_* values.
+SCHEDULES = {0: "plain", 1: "split_kv", 2: "stream"}
+
+
+def schedule(B, Hq, Hkv, Nq, Nkv, D, causal):
+    """How the forward runs this shape on the current device:
+    ``{"kind": "plain" | "split_kv" | "stream", "ctas", "pieces",
+    "blocks_per_cta"}`` (``fa_fwd_schedule``)."""
+    out = [ctypes.c_int(0) for _ in range(4)]
+    st = int(load().fa_fwd_schedule(B, Hq, Hkv, Nq, Nkv, D,
+                                    1 if causal else 0,
+                                    *[ctypes.byref(o) for o in out]))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_schedule")
+    kind, ctas, pieces, bpc = (int(o.value) for o in out)
+    return {"kind": SCHEDULES[kind], "ctas": ctas, "pieces": pieces,
+            "blocks_per_cta": bpc}
+
+
+_SCHEDULE_CODES = {"auto": -1, "plain": 0, "stream": 2}
+
+
+def set_schedule(kind):
+    """Force the schedule of later calls process-wide: ``"auto"`` (the
+    default), ``"plain"`` or ``"stream"`` (``fa_set_schedule``).  Clears the
+    workspace-size cache, whose answers depend on it."""
+    st = int(load().fa_set_schedule(_SCHEDULE_CODES[kind]))
+    if st != FA_OK:
+        raise FAError(st, "fa_set_schedule")
+    _ws_cache.clear()
 
 
 def workspace_size(B, Hq, Hkv, Nq, Nkv, D, causal):

@@ -25,7 +25,8 @@
  *
  * All functions are thread-safe and callable from any host thread.  Device
  * memory: fa_fwd may take stream-ordered scratch from a per-device pool for
- * the split-KV schedule (see fa_fwd_ws); nothing else is allocated.
+ * the split-KV and stream schedules (see fa_fwd_ws and fa_fwd_schedule);
+ * nothing else is allocated.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -92,8 +93,10 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * search page, second snippet).  Each piece leaves fp32 partial results
  * (unnormalised O, running max, running sum per row) in scratch memory and
  * a merge kernel combines them with the same rescaling the online softmax
- * uses between key/value tiles.  fa_fwd takes that scratch from a
- * per-device stream-ordered pool; fa_fwd_ws uses `workspace` instead.
+ * uses between key/value tiles.  The stream schedule (see fa_fwd_schedule)
+ * also needs scratch: one fp32 partial slot and eight flags per CTA.
+ * fa_fwd takes that scratch from a per-device stream-ordered pool;
+ * fa_fwd_ws uses `workspace` instead.
  *
  *   workspace        device pointer, 16-byte aligned, at least
  *                    fa_fwd_workspace_size() bytes; may be NULL when that
@@ -142,6 +145,66 @@ int fa_fwd_qk8(const void* q8, const void* k8, const void* v, void* o,
                float* lse, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
                float scale, float q_descale, float k_descale, int causal,
                void* stream);
+
+/* Schedules reported by fa_fwd_schedule (and forced by fa_set_schedule). */
+enum {
+    FA_SCHEDULE_AUTO = -1,    /* fa_set_schedule only: choose per shape    */
+    FA_SCHEDULE_PLAIN = 0,    /* one CTA per unit of query rows            */
+    FA_SCHEDULE_SPLIT_KV = 1, /* key/value ranges split over CTAs, merged
+                                 by a second kernel (see fa_fwd_ws)        */
+    FA_SCHEDULE_STREAM = 2    /* equal share of all work per CTA           */
+};
+
+/*
+ * fa_fwd_schedule — how fa_fwd, fa_fwd_ws, fa_fwd_qk8 and fa_fwd_noalloc run
+ * this shape on the current device (the choice depends only on the shape
+ * and the device's SM count).
+ *
+ *   *kind            FA_SCHEDULE_PLAIN: one CTA per unit of query rows (a
+ *                    pair of 128-row tiles; one tile for D 192/256 and for
+ *                    causal D 64), each over all its keys;
+ *                    FA_SCHEDULE_SPLIT_KV: each unit's key/value blocks cut
+ *                    into *pieces ranges, one CTA each, then a merge kernel;
+ *                    FA_SCHEDULE_STREAM (no causal mask, D 64 or 128): the
+ *                    (tile pair, key/value block) items of the whole call
+ *                    dealt out in equal contiguous runs of *blocks_per_cta,
+ *                    one per CTA, when whole pairs would leave SMs idle in
+ *                    their last wave.  A pair cut between CTAs is finished
+ *                    by the CTA holding its last block, which combines the
+ *                    others' fp32 partials in its epilogue (no second
+ *                    kernel).  It relies on CTAs being started in index
+ *                    order; a wait that runs out reports FA_ERR_TIMEOUT
+ *                    through fa_last_device_error.
+ *   *ctas            CTAs of the attention kernel
+ *   *pieces          key/value ranges per unit (split-KV), else 1
+ *   *blocks_per_cta  128-key blocks per CTA (stream), else 0
+ * Non-causal grouped-query shapes are counted as they run: the Hq / Hkv
+ * query heads of a group form one head of (Hq / Hkv) * Nq rows.  Argument
+ * errors as fa_fwd_workspace_size; all four outputs must be non-NULL.
+ */
+int fa_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                    int causal, int* kind, int* ctas, int* pieces,
+                    int* blocks_per_cta);
+
+/*
+ * fa_set_schedule — force the schedule of later calls, process-wide, for
+ * testing and tuning (the default, FA_SCHEDULE_AUTO, chooses per shape from
+ * an estimate of each schedule's time).
+ *
+ *   FA_SCHEDULE_PLAIN   one CTA per unit of query rows; also no split-KV
+ *   FA_SCHEDULE_STREAM  the stream schedule wherever it exists (no causal
+ *                       mask, D 64 or 128), with any share per CTA, so a
+ *                       pair may be cut into many pieces; other shapes keep
+ *                       the automatic choice
+ *   FA_SCHEDULE_AUTO    back to the automatic choice
+ *
+ * Returns FA_ERR_INVALID_VALUE for any other value.  The setting is one
+ * atomic word read when a call plans its launch (and by
+ * fa_fwd_workspace_size and fa_fwd_schedule): a workspace sized under one
+ * setting may be too small under another.  Results agree with the oracle
+ * under every setting; only the time and the scratch size change.
+ */
+int fa_set_schedule(int kind);
 
 /* Size of the fixed scratch array behind fa_fwd_noalloc (32 MiB). */
 #define FA_NOALLOC_SCRATCH_BYTES (32u << 20)

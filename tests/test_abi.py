@@ -113,3 +113,12 @@ def test_noalloc_limit_matches_header():
                   text)
     assert m is not None
     assert int(m.group(1)) << int(m.group(2)) == fa.NOALLOC_SCRATCH_BYTES
+
+
+def test_set_schedule_validates_its_argument(lib):
+    """fa_set_schedule takes FA_SCHEDULE_AUTO (-1), PLAIN (0) or STREAM (2)
+    and rejects anything else without touching the device."""
+    for bad in (-2, 1, 3, 99):
+        assert lib.fa_set_schedule(bad) == 1          # FA_ERR_INVALID_VALUE
+    for good in (2, 0, -1):                           # ends on AUTO
+        assert lib.fa_set_schedule(good) == 0

@@ -217,13 +217,16 @@ def test_split_kv_full(D, causal, Nq, Nkv):
 
 
 def test_split_kv_is_used_for_decode_shapes():
+    def kind(*shape):
+        return fa.schedule(*shape)["kind"]
+    assert kind(1, 8, 8, 128, 32768, 128, False) == "split_kv"
+    assert kind(1, 2, 1, 1, 4096, 64, False) == "split_kv"
     assert fa.workspace_size(1, 8, 8, 128, 32768, 128, False) > 0
-    assert fa.workspace_size(1, 2, 1, 1, 4096, 64, False) > 0
     # causal query row 0 sees one key: nothing worth splitting
+    assert kind(1, 2, 1, 1, 4096, 64, True) == "plain"
     assert fa.workspace_size(1, 2, 1, 1, 4096, 64, True) == 0
     w = WORKLOADS["pages_b1_h8_q4096_kv8192_d128"]
-    assert fa.workspace_size(w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D,
-                             w.causal) == 0
+    assert kind(w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D, w.causal) != "split_kv"
 
 
 def test_split_kv_large_logits_and_gqa():
