@@ -92,6 +92,14 @@ WORKLOADS = {
         # The pages' shape with e4m3 Q and K (per-tensor descales).
         Workload("qk8_b1_h8_q4096_kv8192_d128", 1, 8, 8, 4096, 8192, 128,
                  False, qk8=True),
+        # The pages' shape with 5 heads: 80 tile pairs fill 53% of the 152
+        # SMs, so the stream schedule (equal K/V-block shares per CTA) runs
+        # it.  Not one of the pages' shapes; it measures that schedule.
+        Workload("stream_b1_h5_q4096_kv8192_d128", 1, 5, 5, 4096, 8192, 128,
+                 False),
+        # 200 tile pairs (1.3 waves of one pair per SM): stream schedule.
+        Workload("stream_b1_h25_q2048_kv8192_d128", 1, 25, 25, 2048, 8192,
+                 128, False),
     ]
 }
 

@@ -174,10 +174,11 @@ def test_workload_full_size_sampled(name):
 
 @pytest.mark.parametrize("name", ["pages_b1_h8_q4096_kv8192_d128",
                                   "causal_b4_h16_n2048_d64",
-                                  "wide_b1_h8_q4096_kv8192_d256"])
+                                  "wide_b1_h8_q4096_kv8192_d256",
+                                  "stream_b1_h5_q4096_kv8192_d128"])
 def test_workload_full_compare_some_heads(name):
-    """Whole heads of the headline, D=64 and D=256 workloads, element by
-    element."""
+    """Whole heads of the headline, D=64, D=256 and stream-schedule
+    workloads, element by element."""
     w = WORKLOADS[name]
     q, k, v = make_inputs(w)
     o, lse = run_gpu(q, k, v, w.scale, w.causal)
