@@ -376,8 +376,8 @@ int launch_merge(const fa::FwdParams& p, int B, int Hq, int Nq,
 
 template <int D, bool CAUSAL, bool QK8 = false>
 int launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-           const fa::FwdParams& p, int B, int Hq, int Nq,
-           cudaStream_t stream) {
+           const CUtensorMap& o, const fa::FwdParams& p, int B, int Hq,
+           int Nq, cudaStream_t stream) {
   constexpr int kSmem = fa::FwdCfg<D, QK8>::kSmemBytes;
   const int rows_per_cta = fa::kBM * fa::kTilesPerCta;
   const int pairs = (Nq + rows_per_cta - 1) / rows_per_cta;
@@ -389,17 +389,17 @@ int launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
           (total + p.stream_len - 1) / p.stream_len));
       fa::fa_fwd_stream_kernel<D, QK8>
           <<<sgrid, fa::kThreads, fa::StreamCfg<D, QK8>::kSmemBytes,
-             stream>>>(q, k, v, p);
+             stream>>>(q, k, v, o, p);
       return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
     }
   }
   dim3 grid(pairs, Hq, B * p.kv_splits);
   if (p.kv_splits > 1)
     fa::fa_fwd_kernel<D, CAUSAL, true, QK8>
-        <<<grid, fa::kThreads, kSmem, stream>>>(q, k, v, p);
+        <<<grid, fa::kThreads, kSmem, stream>>>(q, k, v, o, p);
   else
     fa::fa_fwd_kernel<D, CAUSAL, false, QK8>
-        <<<grid, fa::kThreads, kSmem, stream>>>(q, k, v, p);
+        <<<grid, fa::kThreads, kSmem, stream>>>(q, k, v, o, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   if (p.kv_splits > 1) return launch_merge<D, fa::kBM * fa::kTilesPerCta>(
                                 p, B, Hq, Nq, stream);
@@ -534,7 +534,7 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
     }
   }
 
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const int kv_rows = one_tile(D, causal) ? fa::WideCfg<256>::kBN : fa::kBN;
   const bool qk_ok =
       qk8 ? (encode_bhnd_e4m3(&tq, q, static_cast<long long>(B) * Hq, Nq,
@@ -545,15 +545,17 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
                  FA_OK &&
              encode_bhnd(&tk, k, static_cast<long long>(B) * Hkv, Nkv, D,
                          kv_rows) == FA_OK);
+  // O: written by the two-tile kernels' TMA stores in boxes of 32 rows
   if ((st = qk_ok ? FA_OK : FA_ERR_CUDA) ||
       (st = encode_bhnd(&tv, v, static_cast<long long>(B) * Hkv, Nkv, D,
-                        kv_rows))) {
+                        kv_rows)) ||
+      (st = encode_bhnd(&to, o, static_cast<long long>(B) * Hq, Nq, D, 32))) {
     if (owned != nullptr) cudaFreeAsync(owned, s);
     return st;
   }
   if (qk8)
-    st = causal ? launch<128, true, true>(tq, tk, tv, p, B, Hq, Nq, s)
-                : launch<128, false, true>(tq, tk, tv, p, B, Hq, Nq, s);
+    st = causal ? launch<128, true, true>(tq, tk, tv, to, p, B, Hq, Nq, s)
+                : launch<128, false, true>(tq, tk, tv, to, p, B, Hq, Nq, s);
   else if (D == 256)
     st = causal ? launch_wide<256, true>(tq, tk, tv, p, B, Hq, Nq, s)
                 : launch_wide<256, false>(tq, tk, tv, p, B, Hq, Nq, s);
@@ -564,11 +566,11 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
     st = causal ? launch_wide<64, true>(tq, tk, tv, p, B, Hq, Nq, s)
                 : launch_wide<64, false>(tq, tk, tv, p, B, Hq, Nq, s);
   else if (D == 64)
-    st = causal ? launch<64, true>(tq, tk, tv, p, B, Hq, Nq, s)
-                : launch<64, false>(tq, tk, tv, p, B, Hq, Nq, s);
+    st = causal ? launch<64, true>(tq, tk, tv, to, p, B, Hq, Nq, s)
+                : launch<64, false>(tq, tk, tv, to, p, B, Hq, Nq, s);
   else
-    st = causal ? launch<128, true>(tq, tk, tv, p, B, Hq, Nq, s)
-                : launch<128, false>(tq, tk, tv, p, B, Hq, Nq, s);
+    st = causal ? launch<128, true>(tq, tk, tv, to, p, B, Hq, Nq, s)
+                : launch<128, false>(tq, tk, tv, to, p, B, Hq, Nq, s);
   if (owned != nullptr && cudaFreeAsync(owned, s) != cudaSuccess &&
       st == FA_OK)
     st = FA_ERR_CUDA;

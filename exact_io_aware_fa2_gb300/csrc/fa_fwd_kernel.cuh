@@ -109,6 +109,18 @@ struct FwdCfg {
       static_cast<int64_t>(kTilesPerCta * kBM) * (D + 2);
 };
 
+// The K ring holds the staged output rows of all eight softmax warps
+// (32 rows x D bf16 each) once the last S MMA has read it.
+template <int D, bool QK8>
+constexpr bool k_ring_holds_output() {
+  return 8 * 32 * D * 2 <=
+         FwdCfg<D, QK8>::kKStages * FwdCfg<D, QK8>::kQKTileBytes;
+}
+static_assert(k_ring_holds_output<64, false>() &&
+                  k_ring_holds_output<128, false>() &&
+                  k_ring_holds_output<128, true>(),
+              "output staging");
+
 struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
@@ -326,16 +338,77 @@ __device__ __forceinline__ void softmax_block(
   tc_fence_before();
 }
 
+// Where a warp's finished rows go.  smem == 0: each lane stores its own row
+// (one 16-byte store per 8 columns; a warp's store then touches 32 rows).
+// Otherwise smem is free, 1024-byte aligned shared memory of 32 * D * 2
+// bytes: the 32 rows are staged there as D/64 boxes of 32 rows x 128 bytes in
+// the 128-byte swizzle (16-byte chunk k of row r at position k ^ (r & 7), so
+// eight lanes' stores hit distinct banks) and one lane writes the boxes with
+// TMA stores through `map` (the O tensor, boxes of 64 columns x 32 rows),
+// starting at row row0 of slice z, whose rows run to n; rows past n are
+// dropped by the TMA unit, and a warp whose rows all lie past n stores
+// nothing.
+struct OutRows {
+  uint32_t smem;
+  const CUtensorMap* map;
+  int row0, z, n;
+};
+
+template <int D>
+__device__ __forceinline__ void put_row_chunk(const OutRows& out, int lane,
+                                              int cc, const uint32_t* packed,
+                                              __nv_bfloat16* orow,
+                                              bool in_range) {
+  if (out.smem != 0) {
+    const uint32_t row = out.smem + (cc >> 1) * (32 * 128) +
+                         static_cast<uint32_t>(lane) * 128;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t k = static_cast<uint32_t>((cc & 1) * 4 + i);
+      st_shared_v4(row + ((k ^ static_cast<uint32_t>(lane & 7)) << 4),
+                   packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                   packed[4 * i + 3]);
+    }
+  } else if (in_range) {
+    uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1],
+                          packed[4 * i + 2], packed[4 * i + 3]);
+  }
+}
+
+// After every lane has put all its chunks: write the staged boxes (no-op for
+// direct stores).  Returns once the TMA unit has read the shared memory.
+template <int D>
+__device__ __forceinline__ void flush_rows(const OutRows& out, int lane) {
+  if (out.smem == 0) return;
+  fence_async_smem();
+  __syncwarp();
+  if (lane == 0 && out.row0 < out.n) {
+#pragma unroll
+    for (int box = 0; box < D / 64; ++box)
+      tma_store_3d(out.map, out.smem + box * (32 * 128), box * 64, out.row0,
+                   out.z);
+    tma_store_commit();
+    tma_store_wait_read();
+  }
+  __syncwarp();
+}
+
 // The last step for one query row: O (unnormalised, in TMEM at o_addr,
 // relative to the reference max m_ref) divided by the row sum l_run, rounded
-// to bf16 and stored at orow; LSE = (m_ref + log2 l_run) ln 2 at lse_at
-// (skipped when null).  Rows past the end (`in_range` false) store nothing.
+// to bf16 and stored (see OutRows; orow is the row's address for direct
+// stores); LSE = (m_ref + log2 l_run) ln 2 at lse_at (skipped when null).
+// Rows past the end (`in_range` false) store nothing.
 template <int D>
 __device__ __forceinline__ void store_final_row(uint32_t o_addr, float m_ref,
                                                 float l_run,
                                                 __nv_bfloat16* orow,
-                                                float* lse_at, bool in_range) {
+                                                float* lse_at, bool in_range,
+                                                const OutRows& out) {
   const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+  const int lane = static_cast<int>(threadIdx.x & 31);
 #pragma unroll
   for (int cc = 0; cc < D / 32; ++cc) {
     uint32_t orr[32];
@@ -347,14 +420,9 @@ __device__ __forceinline__ void store_final_row(uint32_t o_addr, float m_ref,
     for (int i = 0; i < 16; ++i)
       packed[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
                               __uint_as_float(orr[2 * i + 1]) * inv_l);
-    if (in_range) {
-      uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1],
-                            packed[4 * i + 2], packed[4 * i + 3]);
-    }
+    put_row_chunk<D>(out, lane, cc, packed, orow, in_range);
   }
+  flush_rows<D>(out, lane);
   if (in_range && lse_at != nullptr) {
     const float lse2 = (l_run > 0.f) ? (m_ref + log2f(l_run)) : -INFINITY;
     *lse_at = lse2 * 0.69314718055994530942f;
@@ -369,6 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmO,
                   const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D, QK8>;
   constexpr int NK = C::kKStages;
@@ -618,10 +687,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t row_idx =
           (static_cast<size_t>(b) * p.Hq + hq) * static_cast<size_t>(p.Nq) +
           static_cast<size_t>(q_abs);
+      // Every MMA is complete and every K tile consumed: the K ring is free
+      // shared memory for staging the rows (8 warps x 32 rows x D bf16 fit
+      // in it at both head dims).
+      const int role = warp - kSoftmaxWarp0;
+      const OutRows out{sK + static_cast<uint32_t>(role) * (32u * D * 2u),
+                        &tmO, my_row0 + (warp & 3) * 32, b * p.Hq + hq, p.Nq};
       store_final_row<D>(tmem + lane_off + C::col_o(x), m_ref, l_run,
                          p.o + row_idx * D,
                          p.lse != nullptr ? p.lse + row_idx : nullptr,
-                         q_abs < p.Nq);
+                         q_abs < p.Nq, out);
     }
     }
   }

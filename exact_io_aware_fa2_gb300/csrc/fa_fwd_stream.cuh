@@ -137,12 +137,14 @@ __device__ __forceinline__ void publish_partial(uint64_t* flag, uint64_t epoch,
 
 // The merger's last step for one row: combine its own accumulator (TMEM at
 // o_addr, reference max m_own, sum l_own) with the partials of CTAs
-// k0 .. k1-1 for the same row (prow within the pair), then store the row and
-// its LSE as store_final_row does.
+// k0 .. k1-1 for the same row (prow within the pair), then store the row
+// (see OutRows) and its LSE as store_final_row does.
 template <int D>
 __device__ __forceinline__ void merge_final_row(
     uint32_t o_addr, float m_own, float l_own, const float* work, int k0,
-    int k1, int prow, __nv_bfloat16* orow, float* lse_at, bool in_range) {
+    int k1, int prow, __nv_bfloat16* orow, float* lse_at, bool in_range,
+    const OutRows& out) {
+  const int lane = static_cast<int>(threadIdx.x & 31);
   constexpr int64_t kSlot = stream_slot_floats<D>();
   constexpr int kRows = kTilesPerCta * kBM;
   // Start every load this row needs at once (into L1), so the loop below
@@ -192,18 +194,13 @@ __device__ __forceinline__ void merge_final_row(
         acc[4 * i + 3] += wk * v.w;
       }
     }
-    if (in_range) {
-      uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+    uint32_t packed[16];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float* a = acc + 8 * i;
-        dst[i] = make_uint4(pack_bf16x2(a[0] * inv_l, a[1] * inv_l),
-                            pack_bf16x2(a[2] * inv_l, a[3] * inv_l),
-                            pack_bf16x2(a[4] * inv_l, a[5] * inv_l),
-                            pack_bf16x2(a[6] * inv_l, a[7] * inv_l));
-      }
-    }
+    for (int i = 0; i < 16; ++i)
+      packed[i] = pack_bf16x2(acc[2 * i] * inv_l, acc[2 * i + 1] * inv_l);
+    put_row_chunk<D>(out, lane, cc, packed, orow, in_range);
   }
+  flush_rows<D>(out, lane);
   if (in_range && lse_at != nullptr) {
     const float lse2 = (l > 0.f) ? (M + log2f(l)) : -INFINITY;
     *lse_at = lse2 * 0.69314718055994530942f;
@@ -223,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_stream_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmO,
                          const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D, QK8>;
   using SC = StreamCfg<D, QK8>;
@@ -512,8 +510,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __nv_bfloat16* const orow = p.o + row_idx * D;
         float* const lse_at = p.lse != nullptr ? p.lse + row_idx : nullptr;
         const bool in_range = q_abs < p.Nq;
+        // In the CTA's last segment every MMA is complete and every K tile
+        // consumed: the K ring stages the output rows for TMA stores.
+        const OutRows out{
+            si + 1 == n_seg ? sK + static_cast<uint32_t>(role) * (32u * D * 2u)
+                            : 0u,
+            &tmO, my_row0 + (warp & 3) * 32, sg.b * p.Hq + sg.hq, p.Nq};
         if (sg.kind == kSegWhole) {
-          store_final_row<D>(o_addr, m_ref, l_run, orow, lse_at, in_range);
+          store_final_row<D>(o_addr, m_ref, l_run, orow, lse_at, in_range,
+                             out);
         } else if (sg.kind == kSegWriter) {
           float* const slot = p.work + static_cast<int64_t>(blockIdx.x) * kSlot;
           float4* const so = reinterpret_cast<float4*>(slot);
@@ -550,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           p.epoch, wc));
           if (ok) {
             merge_final_row<D>(o_addr, m_ref, l_run, p.work, sg.first_cta,
-                               k1, prow, orow, lse_at, in_range);
+                               k1, prow, orow, lse_at, in_range, out);
             // Consumed: clear the flags so that a replay of this launch
             // waits for its own writers again.
             __syncwarp();
