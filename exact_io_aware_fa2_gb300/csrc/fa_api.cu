@@ -408,17 +408,18 @@ int launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
 
 template <int D, bool CAUSAL>
 int launch_wide(const CUtensorMap& q, const CUtensorMap& k,
-                const CUtensorMap& v, const fa::FwdParams& p, int B, int Hq,
-                int Nq, cudaStream_t stream) {
+                const CUtensorMap& v, const CUtensorMap& o,
+                const fa::FwdParams& p, int B, int Hq, int Nq,
+                cudaStream_t stream) {
   dim3 grid((Nq + fa::kBM - 1) / fa::kBM, Hq, B * p.kv_splits);
   if (p.kv_splits > 1)
     fa::fa_fwd_wide_kernel<D, CAUSAL, true>
         <<<grid, fa::kWideThreads, fa::WideCfg<D>::kSmemBytes, stream>>>(
-            q, k, v, p);
+            q, k, v, o, p);
   else
     fa::fa_fwd_wide_kernel<D, CAUSAL, false>
         <<<grid, fa::kWideThreads, fa::WideCfg<D>::kSmemBytes, stream>>>(
-            q, k, v, p);
+            q, k, v, o, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   if (p.kv_splits > 1)
     return launch_merge<D, fa::kBM>(p, B, Hq, Nq, stream);
@@ -545,7 +546,7 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
                  FA_OK &&
              encode_bhnd(&tk, k, static_cast<long long>(B) * Hkv, Nkv, D,
                          kv_rows) == FA_OK);
-  // O: written by the two-tile kernels' TMA stores in boxes of 32 rows
+  // O: written by the kernels' TMA stores in boxes of 32 rows
   if ((st = qk_ok ? FA_OK : FA_ERR_CUDA) ||
       (st = encode_bhnd(&tv, v, static_cast<long long>(B) * Hkv, Nkv, D,
                         kv_rows)) ||
@@ -557,14 +558,14 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
     st = causal ? launch<128, true, true>(tq, tk, tv, to, p, B, Hq, Nq, s)
                 : launch<128, false, true>(tq, tk, tv, to, p, B, Hq, Nq, s);
   else if (D == 256)
-    st = causal ? launch_wide<256, true>(tq, tk, tv, p, B, Hq, Nq, s)
-                : launch_wide<256, false>(tq, tk, tv, p, B, Hq, Nq, s);
+    st = causal ? launch_wide<256, true>(tq, tk, tv, to, p, B, Hq, Nq, s)
+                : launch_wide<256, false>(tq, tk, tv, to, p, B, Hq, Nq, s);
   else if (D == 192)
-    st = causal ? launch_wide<192, true>(tq, tk, tv, p, B, Hq, Nq, s)
-                : launch_wide<192, false>(tq, tk, tv, p, B, Hq, Nq, s);
+    st = causal ? launch_wide<192, true>(tq, tk, tv, to, p, B, Hq, Nq, s)
+                : launch_wide<192, false>(tq, tk, tv, to, p, B, Hq, Nq, s);
   else if (D == 64 && one_tile(D, causal))
-    st = causal ? launch_wide<64, true>(tq, tk, tv, p, B, Hq, Nq, s)
-                : launch_wide<64, false>(tq, tk, tv, p, B, Hq, Nq, s);
+    st = causal ? launch_wide<64, true>(tq, tk, tv, to, p, B, Hq, Nq, s)
+                : launch_wide<64, false>(tq, tk, tv, to, p, B, Hq, Nq, s);
   else if (D == 64)
     st = causal ? launch<64, true>(tq, tk, tv, to, p, B, Hq, Nq, s)
                 : launch<64, false>(tq, tk, tv, to, p, B, Hq, Nq, s);

@@ -78,6 +78,8 @@ struct WideCfg {
   // relative to the slot's reference max), then m[128], then l[128].
   static constexpr int64_t kSlotFloats = static_cast<int64_t>(kBM) * (D + 2);
   static constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
+  // the K ring holds the four softmax warps' staged output rows
+  static_assert(4 * 32 * D * 2 <= kKStages * kKVBytes, "output staging");
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);
 };
 
@@ -123,6 +125,7 @@ __global__ void __launch_bounds__(kWideThreads, WideCfg<D>::kCtasPerSm)
     fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmO,
                        const __grid_constant__ FwdParams p) {
   using W = WideCfg<D>;
   constexpr int BN = W::kBN;
@@ -466,35 +469,16 @@ __global__ void __launch_bounds__(kWideThreads, WideCfg<D>::kCtasPerSm)
       slot[kBM * D + kBM + trow] = nblk > 0 ? l_run : 0.f;
     } else if (ok && nblk > 0) {
       tc_fence_after();
-      const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      const bool in_range = q_abs < p.Nq;
       const size_t row_idx =
           (static_cast<size_t>(b) * p.Hq + hq) * static_cast<size_t>(p.Nq) +
           static_cast<size_t>(q_abs);
-      __nv_bfloat16* orow = p.o + row_idx * D;
-#pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t orr[32];
-        tmem_ld32(o_addr + cc * 32, orr);
-        tmem_ld_wait();
-        reg_fence32(orr);
-        uint32_t packed[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          packed[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
-                                  __uint_as_float(orr[2 * i + 1]) * inv_l);
-        if (in_range) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1],
-                                packed[4 * i + 2], packed[4 * i + 3]);
-        }
-      }
-      if (in_range && p.lse != nullptr) {
-        const float lse2 = (l_run > 0.f) ? (m_ref + log2f(l_run)) : -INFINITY;
-        p.lse[row_idx] = lse2 * 0.69314718055994530942f;
-      }
+      // Every MMA is complete and every K tile consumed: the K ring stages
+      // the four warps' rows for TMA stores.
+      const OutRows out{sK + static_cast<uint32_t>(warp & 3) * (32u * D * 2u),
+                        &tmO, q_abs - lane, b * p.Hq + hq, p.Nq};
+      store_final_row<D>(o_addr, m_ref, l_run, p.o + row_idx * D,
+                         p.lse != nullptr ? p.lse + row_idx : nullptr,
+                         q_abs < p.Nq, out);
     }
   }
 
