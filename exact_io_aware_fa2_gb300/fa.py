@@ -28,7 +28,7 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_VALUE", 2: "FA_ERR_UNSUPPORTED",
                 3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
 # Every symbol the header declares.
 SYMBOLS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_noalloc",
-           "fa_fwd_qk8", "fa_fwd_schedule", "fa_set_schedule",
+           "fa_fwd_qk8", "fa_fwd_schedule", "fa_set_schedule", "fa_fwd_host",
            "fa_status_string", "fa_last_device_error",
            "fa_probe_bounded_wait", "fa_version")
 
@@ -88,6 +88,9 @@ def load():
         lib.fa_fwd_schedule.restype = ci
         lib.fa_set_schedule.argtypes = [ci]
         lib.fa_set_schedule.restype = ci
+        lib.fa_fwd_host.argtypes = [vp] * 10 + [ci] * 6 + [ctypes.c_float,
+                                                          ci, vp]
+        lib.fa_fwd_host.restype = ci
         _lib = lib
         return lib
 
@@ -118,6 +121,13 @@ def _check(q, k, v):
     if k.shape != v.shape or k.shape[0] != B or k.shape[3] != D:
         raise ValueError("k, v must be [B, Hkv, Nkv, D] matching q")
     return B, Hq, k.shape[1], Nq, k.shape[2], D
+
+
+def _check_host(q, k, v):
+    _check(q, k, v)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.device.type != "cpu":
+            raise ValueError(f"{name} must be a host (CPU) tensor")
 
 
 def fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, Nq, Nkv, D,
@@ -289,24 +299,35 @@ def fwd_qk8(q8, k8, v, scale=None, q_descale=1.0, k_descale=1.0,
 
 
 def fwd_host(q, k, v, scale=None, causal=False, device="cuda", bufs=None):
-    """Forward on host tensors: copy in (pinned -> device), run, copy out.
+    """Forward on host tensors through ``fa_fwd_host``: the library copies
+    Q, K, V in, runs the forward and copies O and LSE out, overlapping the
+    copies with the computation chunk by chunk.
 
-    ``bufs`` may hold preallocated device buffers (q, k, v, o, lse) and
-    pinned host outputs (o_h, lse_h) to reuse across calls.  Returns host
-    (o, lse); the copies and the kernel are ordered on the current stream,
-    and the call synchronises that stream before returning.
+    ``q, k, v`` are CPU bf16 tensors (page-locked for the copies to
+    overlap).  ``bufs`` may hold preallocated device buffers (q, k, v, o,
+    lse) and pinned host outputs (o_h, lse_h) to reuse across calls
+    (``host_buffers``).  Returns the host (o, lse); the call synchronises
+    the current stream before returning.
     """
-    _check(q, k, v)
+    _check_host(q, k, v)
     if bufs is None:
         bufs = host_buffers(q, k, v, device)
-    bufs["q"].copy_(q, non_blocking=True)
-    bufs["k"].copy_(k, non_blocking=True)
-    bufs["v"].copy_(v, non_blocking=True)
-    fwd(bufs["q"], bufs["k"], bufs["v"], scale=scale, causal=causal,
-        out=bufs["o"], lse=bufs["lse"])
-    bufs["o_h"].copy_(bufs["o"], non_blocking=True)
-    bufs["lse_h"].copy_(bufs["lse"], non_blocking=True)
-    torch.cuda.current_stream(bufs["o"].device).synchronize()
+    B, Hq, Nq, D = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dev = bufs["o"].device
+    stream = torch.cuda.current_stream(dev)
+    p = [t.data_ptr() for t in (q, k, v, bufs["o_h"], bufs["lse_h"],
+                                bufs["q"], bufs["k"], bufs["v"], bufs["o"],
+                                bufs["lse"])]
+    st = int(load().fa_fwd_host(*[ctypes.c_void_p(x) for x in p], B, Hq, Hkv,
+                                Nq, Nkv, D, ctypes.c_float(scale),
+                                1 if causal else 0,
+                                ctypes.c_void_p(stream.cuda_stream)))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_host")
+    stream.synchronize()
     return bufs["o_h"], bufs["lse_h"]
 
 

@@ -206,6 +206,43 @@ int fa_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
  */
 int fa_set_schedule(int kind);
 
+/*
+ * fa_fwd_host — fa_fwd on host buffers: copies Q, K, V in, runs the forward,
+ * copies O and LSE out, overlapping the copies with the computation.
+ *
+ * The pages describe no such call; host-resident inputs are where a caller
+ * without device-side producers starts, and the host link is slower than
+ * the forward (on GB300 about 200 GB/s each way: 42 MB of bf16 Q, K, V for
+ * the 4096 x 8192 x 8-head shape take 0.2 ms, twice the forward).  The call
+ * splits the job into at most 4 chunks of consecutive (batch, kv head)
+ * groups, each a forward of its own (a group's rows are contiguous in the
+ * [B, H, N, D] layout): chunk c's K, V and Q are copied in on a side stream,
+ * its forward runs on `stream` (its small size lets the split-KV schedule
+ * spread it over the GPU), and its O and LSE are copied out on a second side
+ * stream while later chunks copy in and compute.
+ *
+ *   q_host, k_host, v_host  host pointers, layouts as fa_fwd's q, k, v; page-
+ *                           locked (cudaHostAlloc / cudaHostRegister) for the
+ *                           copies to be asynchronous and overlap
+ *   o_host, lse_host        host pointers receiving O and LSE; lse_host may
+ *                           be NULL exactly when lse_dev is NULL
+ *   q_dev .. lse_dev        device buffers of the full sizes, as fa_fwd's
+ *                           arguments (16-byte aligned; lse 4-byte aligned)
+ *   B .. causal             as fa_fwd
+ *   stream                  the work is ordered after the caller's earlier
+ *                           work on `stream`, and `stream` completes only
+ *                           after the last copy out: synchronise it before
+ *                           reading o_host
+ * Errors as fa_fwd; FA_ERR_INVALID_VALUE for a NULL host pointer.  Calls
+ * from different host threads on one device are serialised while they
+ * enqueue (they share the side streams); their GPU work may still overlap.
+ */
+int fa_fwd_host(const void* q_host, const void* k_host, const void* v_host,
+                void* o_host, float* lse_host, void* q_dev, void* k_dev,
+                void* v_dev, void* o_dev, float* lse_dev, int B, int Hq,
+                int Hkv, int Nq, int Nkv, int D, float scale, int causal,
+                void* stream);
+
 /* Size of the fixed scratch array behind fa_fwd_noalloc (32 MiB). */
 #define FA_NOALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -141,6 +141,33 @@ def test_host_buffers_path():
     check(o.clone(), lse.clone(), O, L, "host buffers")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_host_path_chunks_of_groups(causal):
+    """fa_fwd_host cuts the job into at most 4 chunks of (batch, kv head)
+    groups (here 12 groups of 3 query heads: chunks of three groups),
+    copying each chunk in and out around its own forward; every row must
+    land in its place, for GQA, a batch, ragged sizes and the causal mask."""
+    q, k, v = make_custom(3, 12, 4, 333, 457, 64, seed=15)
+    qp, kp, vp = (t.pin_memory() for t in (q, k, v))
+    o, lse = fa.fwd_host(qp, kp, vp, scale=0.125, causal=causal)
+    O, L = oracle.attention_fp64(q, k, v, 0.125, causal)
+    print(check(o.clone(), lse.clone(), O, L, f"host chunks causal={causal}"))
+
+
+def test_host_path_reuses_buffers_and_accepts_pageable_memory():
+    bufs = None
+    for seed, pin in ((16, True), (17, False)):
+        q, k, v = make_custom(2, 8, 2, 256, 700, 128, seed=seed)
+        if pin:
+            q, k, v = (t.pin_memory() for t in (q, k, v))
+        if bufs is None:
+            bufs = fa.host_buffers(q, k, v)
+        o, lse = fa.fwd_host(q, k, v, scale=0.0883883, causal=False,
+                             bufs=bufs)
+        O, L = oracle.attention_fp64(q, k, v, 0.0883883, False)
+        check(o.clone(), lse.clone(), O, L, f"host reuse seed {seed}")
+
+
 # ------------------------------------------------------------- full-size
 
 def _sample_rows(Nq, gen, extra=16):
