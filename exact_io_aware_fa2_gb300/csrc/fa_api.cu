@@ -217,23 +217,23 @@ int plan_splits(int B, int Hq, int Nq, int Nkv, int D, int causal, int sms) {
 // when whole tile pairs leave SMs idle in their last wave, give every CTA
 // an equal contiguous share of all (pair, K/V block) items instead.  Costs
 // in units of one K/V block of one pair on the two-tile kernel, fitted to
-// GB300 timings of both schedules (D = 128, 8192 keys; 80 to 256 pairs;
-// 2048 keys for short rows):
+// GB300 timings of both schedules (D = 128; 80 to 256 pairs; 2048, 4096 and
+// 8192 keys; D = 64 checked):
 //   plain  = waves x blocks per pair + kPairOverheadBlocks
 //   stream = kStreamBlockFactor x blocks per CTA + kStreamOverheadBlocks
 //            + kSegmentBlocks x (segments per CTA - 1)
-// (the stream kernel's blocks are 4% slower, and its partial writes, merges
-// and segment switches cost about 11 blocks more than the plain kernel's
-// start-up and epilogue).  Stream runs when estimated at least kStreamGain
-// faster and a CTA's share is at least half a pair (a merger then combines
-// at most two partials); measured 26% faster at 80 pairs, 18% at 200, and
-// 8% slower at 128 pairs (128 of 152 SMs busy), which the estimate leaves
-// to the plain kernel.
-constexpr double kPairOverheadBlocks = 7.0;
-constexpr double kStreamBlockFactor = 1.04;
-constexpr double kStreamOverheadBlocks = 18.0;
+// (the stream kernel's blocks are 9% slower, and its partial writes,
+// merges and segment switches cost about 9 blocks more than the plain
+// kernel's start-up and epilogue).  Stream runs when estimated at least
+// kStreamGain faster and a CTA's share is at least half a pair (a merger
+// then combines at most two partials).  Measured, stream against plain:
+// 80 pairs 74.4 vs 98.9 us, 112 pairs 94.8 vs 99.0, 200 pairs 156.3 vs
+// 189.1; plain wins at 128 pairs (99.0 vs 105.1) and on 2048-key rows.
+constexpr double kPairOverheadBlocks = 6.2;
+constexpr double kStreamBlockFactor = 1.09;
+constexpr double kStreamOverheadBlocks = 13.2;
 constexpr double kSegmentBlocks = 2.5;
-constexpr double kStreamGain = 0.97;
+constexpr double kStreamGain = 0.98;
 
 // Schedule forced by fa_set_schedule (FA_SCHEDULE_AUTO: the estimate).
 std::atomic<int> g_forced_schedule{FA_SCHEDULE_AUTO};
