@@ -773,6 +773,15 @@ int fa_fwd_host(const void* q_host, const void* k_host, const void* v_host,
       !ok(cudaStreamWaitEvent(hp.h2d, hp.start, 0)) ||
       !ok(cudaStreamWaitEvent(hp.d2h, hp.start, 0)))
     return FA_ERR_CUDA;
+  // From here on, whatever happens, `stream` is made to wait for both side
+  // streams, so synchronising it covers every copy this call enqueued.
+  auto join = [&](int status) {
+    const bool j = ok(cudaEventRecord(hp.in[0], hp.h2d)) &&
+                   ok(cudaStreamWaitEvent(s, hp.in[0], 0)) &&
+                   ok(cudaEventRecord(hp.d2h_done, hp.d2h)) &&
+                   ok(cudaStreamWaitEvent(s, hp.d2h_done, 0));
+    return status != FA_OK ? status : (j ? FA_OK : FA_ERR_CUDA);
+  };
   for (int c = 0; c < n_chunks; ++c) {
     const int64_t g0 = groups * c / n_chunks, g1 = groups * (c + 1) / n_chunks;
     const int64_t ng = g1 - g0;
@@ -789,7 +798,7 @@ int fa_fwd_host(const void* q_host, const void* k_host, const void* v_host,
                             hp.h2d)) ||
         !ok(cudaEventRecord(hp.in[c], hp.h2d)) ||
         !ok(cudaStreamWaitEvent(s, hp.in[c], 0)))
-      return FA_ERR_CUDA;
+      return join(FA_ERR_CUDA);
     // compute on the caller's stream
     st = run_forward(cptr(q_dev, g0 * q_group), cptr(k_dev, g0 * kv_group),
                      cptr(v_dev, g0 * kv_group), mptr(o_dev, g0 * q_group),
@@ -798,25 +807,22 @@ int fa_fwd_host(const void* q_host, const void* k_host, const void* v_host,
                                         : nullptr,
                      static_cast<int>(ng), G, 1, Nq, Nkv, D, scale, causal,
                      nullptr, 0, true, s);
-    if (st != FA_OK) return st;
+    if (st != FA_OK) return join(st);
     // out: this chunk's O and LSE while later chunks copy in and compute
     if (!ok(cudaEventRecord(hp.done[c], s)) ||
         !ok(cudaStreamWaitEvent(hp.d2h, hp.done[c], 0)) ||
         !ok(cudaMemcpyAsync(mptr(o_host, g0 * q_group),
                             cptr(o_dev, g0 * q_group), ng * q_group,
                             cudaMemcpyDeviceToHost, hp.d2h)))
-      return FA_ERR_CUDA;
+      return join(FA_ERR_CUDA);
     if (lse_host != nullptr &&
         !ok(cudaMemcpyAsync(mptr(lse_host, g0 * lse_group),
                             cptr(lse_dev, g0 * lse_group), ng * lse_group,
                             cudaMemcpyDeviceToHost, hp.d2h)))
-      return FA_ERR_CUDA;
+      return join(FA_ERR_CUDA);
   }
   // The caller's stream completes after the last copy out.
-  if (!ok(cudaEventRecord(hp.d2h_done, hp.d2h)) ||
-      !ok(cudaStreamWaitEvent(s, hp.d2h_done, 0)))
-    return FA_ERR_CUDA;
-  return FA_OK;
+  return join(FA_OK);
 }
 
 int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o,

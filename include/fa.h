@@ -233,9 +233,13 @@ int fa_set_schedule(int kind);
  *                           work on `stream`, and `stream` completes only
  *                           after the last copy out: synchronise it before
  *                           reading o_host
- * Errors as fa_fwd; FA_ERR_INVALID_VALUE for a NULL host pointer.  Calls
- * from different host threads on one device are serialised while they
- * enqueue (they share the side streams); their GPU work may still overlap.
+ * Errors as fa_fwd; FA_ERR_INVALID_VALUE for a NULL host pointer (checked
+ * before anything is enqueued).  If an error occurs after the first copy was
+ * enqueued, `stream` is still made to wait for every copy already enqueued,
+ * so synchronising it is enough before the buffers are reused; the outputs
+ * are then incomplete.  Calls from different host threads on one device are
+ * serialised while they enqueue (they share the side streams); their GPU
+ * work may still overlap.
  */
 int fa_fwd_host(const void* q_host, const void* k_host, const void* v_host,
                 void* o_host, float* lse_host, void* q_dev, void* k_dev,

@@ -122,3 +122,17 @@ def test_set_schedule_validates_its_argument(lib):
         assert lib.fa_set_schedule(bad) == 1          # FA_ERR_INVALID_VALUE
     for good in (2, 0, -1):                           # ends on AUTO
         assert lib.fa_set_schedule(good) == 0
+
+
+def test_host_entry_point_checks_host_pointers_first(lib):
+    """fa_fwd_host rejects a NULL host pointer, or lse_host and lse_dev not
+    both NULL or both set, before touching the device."""
+    dev = [ctypes.c_void_p(256)] * 5
+    host = [ctypes.c_void_p(512)] * 5
+    args = (1, 1, 1, 128, 128, 128, ctypes.c_float(0.1), 0, None)
+    for i in range(4):
+        bad = list(host)
+        bad[i] = None
+        assert lib.fa_fwd_host(*bad, *dev, *args) == 1
+    assert lib.fa_fwd_host(*host[:4], None, *dev, *args) == 1
+    assert lib.fa_fwd_host(*host, *dev[:4], None, *args) == 1
