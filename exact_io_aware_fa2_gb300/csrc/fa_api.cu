@@ -460,6 +460,23 @@ __global__ void probe_wait_kernel(int* status, uint64_t limit_ns) {
   __syncwarp();
 }
 
+// A global-memory flag nothing ever sets, for fa_probe_flag_wait.
+__device__ uint64_t g_probe_flag = 0;
+
+__global__ void probe_flag_kernel(int* status, uint64_t limit_ns) {
+  __shared__ fa::WaitState ws;
+  if (threadIdx.x == 0) {
+    ws.abort = 0;
+    ws.status = status;
+    ws.limit_ns = limit_ns;
+  }
+  __syncwarp();
+  // The value 1 is never published: the wait must run out.
+  const fa::WaitCtx wc{fa::smem_addr(&ws)};
+  fa::flag_wait(&g_probe_flag, 1ull, wc);
+  __syncwarp();
+}
+
 int check_args(const void* q, const void* k, const void* v, const void* o,
                const float* lse, int B, int Hq, int Hkv, int Nq, int Nkv,
                int D, float scale) {
@@ -868,6 +885,16 @@ int fa_probe_bounded_wait(long long timeout_ns, void* stream) {
   int st = device_ready(&word);
   if (st != FA_OK) return st;
   probe_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      word, static_cast<uint64_t>(timeout_ns));
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_probe_flag_wait(long long timeout_ns, void* stream) {
+  if (timeout_ns < 1 || timeout_ns > 1000000000ll) return FA_ERR_INVALID_VALUE;
+  int* word = nullptr;
+  int st = device_ready(&word);
+  if (st != FA_OK) return st;
+  probe_flag_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
       word, static_cast<uint64_t>(timeout_ns));
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

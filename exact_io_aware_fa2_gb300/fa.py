@@ -29,6 +29,7 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_VALUE", 2: "FA_ERR_UNSUPPORTED",
 # Every symbol the header declares.
 SYMBOLS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_noalloc",
            "fa_fwd_qk8", "fa_fwd_schedule", "fa_set_schedule", "fa_fwd_host",
+           "fa_probe_flag_wait",
            "fa_status_string", "fa_last_device_error",
            "fa_probe_bounded_wait", "fa_version")
 
@@ -91,6 +92,8 @@ def load():
         lib.fa_fwd_host.argtypes = [vp] * 10 + [ci] * 6 + [ctypes.c_float,
                                                           ci, vp]
         lib.fa_fwd_host.restype = ci
+        lib.fa_probe_flag_wait.argtypes = [ctypes.c_longlong, vp]
+        lib.fa_probe_flag_wait.restype = ci
         _lib = lib
         return lib
 
@@ -107,6 +110,12 @@ def probe_bounded_wait(timeout_ns, stream=None):
     st = stream if stream is not None else torch.cuda.current_stream()
     return int(load().fa_probe_bounded_wait(int(timeout_ns),
                                             ctypes.c_void_p(st.cuda_stream)))
+
+
+def probe_flag_wait(timeout_ns, stream=None):
+    st = stream if stream is not None else torch.cuda.current_stream()
+    return int(load().fa_probe_flag_wait(int(timeout_ns),
+                                         ctypes.c_void_p(st.cuda_stream)))
 
 
 def _check(q, k, v):

@@ -306,6 +306,17 @@ int fa_last_device_error(void);
  */
 int fa_probe_bounded_wait(long long timeout_ns, void* stream);
 
+/*
+ * fa_probe_flag_wait — as fa_probe_bounded_wait, for the other bounded wait
+ * the kernels use: a one-warp kernel waits (acquire loads) for a global
+ * 64-bit flag to reach a value nothing will ever publish — the wait a stream-
+ * schedule CTA makes for another CTA's partial — with a limit of
+ * `timeout_ns` (1 .. 10^9), then records FA_ERR_TIMEOUT for
+ * fa_last_device_error() and returns.  FA_ERR_INVALID_VALUE for a limit
+ * outside the range.
+ */
+int fa_probe_flag_wait(long long timeout_ns, void* stream);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int fa_version(void);
 

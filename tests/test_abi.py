@@ -93,6 +93,8 @@ def test_lse_may_be_null_for_validation(lib):
 def test_probe_rejects_bad_limits(lib):
     assert lib.fa_probe_bounded_wait(0, None) == 1
     assert lib.fa_probe_bounded_wait(2_000_000_000, None) == 1
+    assert lib.fa_probe_flag_wait(0, None) == 1
+    assert lib.fa_probe_flag_wait(2_000_000_000, None) == 1
 
 
 def test_binding_rejects_bad_tensors():

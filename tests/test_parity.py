@@ -230,6 +230,19 @@ def test_bounded_wait_expires_into_status_and_context_survives():
     full_compare(*make_inputs(w), w.scale, False, "after probe")
 
 
+def test_flag_wait_expires_into_status_and_context_survives():
+    """The stream schedule's wait for another CTA's partial (acquire loads of
+    a global flag) gives up at its limit with FA_ERR_TIMEOUT, like the
+    mbarrier waits; nothing faults and the context stays usable."""
+    assert fa.last_device_error() == 0
+    assert fa.probe_flag_wait(2_000_000) == 0       # 2 ms limit
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 5              # FA_ERR_TIMEOUT
+    assert fa.last_device_error() == 0
+    w = WORKLOADS["tiny_128_d64"]
+    full_compare(*make_inputs(w), w.scale, False, "after flag probe")
+
+
 # ------------------------------------------------ split-KV (few query blocks)
 
 @pytest.mark.parametrize("causal", [False, True])
