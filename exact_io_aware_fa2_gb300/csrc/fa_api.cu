@@ -650,6 +650,34 @@ int fa_set_schedule(int kind) {
   return FA_OK;
 }
 
+int fa_fwd_schedule_for(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                        int causal, int sms, int* kind, int* ctas,
+                        int* pieces, int* blocks_per_cta,
+                        size_t* workspace) {
+  if (kind == nullptr || ctas == nullptr || pieces == nullptr ||
+      blocks_per_cta == nullptr || workspace == nullptr || sms < 1)
+    return FA_ERR_INVALID_VALUE;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nkv < 1 || D < 1 ||
+      Hq % Hkv != 0 || B > 65535 || Hq > 65535)
+    return FA_ERR_INVALID_VALUE;
+  if (!supported_head_dim(D)) return FA_ERR_UNSUPPORTED;
+  const RunShape rs = run_shape(Hq, Hkv, Nq, causal);
+  const Plan pl = plan_forward(B, rs.Hq, rs.Nq, Nkv, D, causal, sms);
+  const int64_t rows_u = unit_rows(D, causal);
+  const int64_t units = (rs.Nq + rows_u - 1) / rows_u;
+  *kind = pl.stream_len > 0 ? FA_SCHEDULE_STREAM
+          : pl.splits > 1   ? FA_SCHEDULE_SPLIT_KV
+                            : FA_SCHEDULE_PLAIN;
+  *ctas = pl.stream_len > 0
+              ? pl.stream_ctas
+              : static_cast<int>(units * rs.Hq * B * pl.splits);
+  *pieces = pl.splits;
+  *blocks_per_cta = pl.stream_len;
+  *workspace = static_cast<size_t>(workspace_bytes(B, rs.Hq, rs.Nq, D,
+                                                   causal, pl));
+  return FA_OK;
+}
+
 int fa_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
                     int causal, int* kind, int* ctas, int* pieces,
                     int* blocks_per_cta) {
@@ -663,20 +691,9 @@ int fa_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
   int dev = 0;
   const int st = device_ready(nullptr, &dev);
   if (st != FA_OK) return st;
-  const RunShape rs = run_shape(Hq, Hkv, Nq, causal);
-  const Plan pl =
-      plan_forward(B, rs.Hq, rs.Nq, Nkv, D, causal, g_sm_count[dev]);
-  const int64_t rows_u = unit_rows(D, causal);
-  const int64_t units = (rs.Nq + rows_u - 1) / rows_u;
-  *kind = pl.stream_len > 0 ? FA_SCHEDULE_STREAM
-          : pl.splits > 1   ? FA_SCHEDULE_SPLIT_KV
-                            : FA_SCHEDULE_PLAIN;
-  *ctas = pl.stream_len > 0
-              ? pl.stream_ctas
-              : static_cast<int>(units * rs.Hq * B * pl.splits);
-  *pieces = pl.splits;
-  *blocks_per_cta = pl.stream_len;
-  return FA_OK;
+  size_t ws = 0;
+  return fa_fwd_schedule_for(B, Hq, Hkv, Nq, Nkv, D, causal, g_sm_count[dev],
+                             kind, ctas, pieces, blocks_per_cta, &ws);
 }
 
 }  // extern "C"

@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_VALUE", 2: "FA_ERR_UNSUPPORTED",
 # Every symbol the header declares.
 SYMBOLS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_noalloc",
            "fa_fwd_qk8", "fa_fwd_schedule", "fa_set_schedule", "fa_fwd_host",
-           "fa_probe_flag_wait",
+           "fa_probe_flag_wait", "fa_fwd_schedule_for",
            "fa_status_string", "fa_last_device_error",
            "fa_probe_bounded_wait", "fa_version")
 
@@ -94,6 +94,9 @@ def load():
         lib.fa_fwd_host.restype = ci
         lib.fa_probe_flag_wait.argtypes = [ctypes.c_longlong, vp]
         lib.fa_probe_flag_wait.restype = ci
+        lib.fa_fwd_schedule_for.argtypes = [ci] * 8 + [pi] * 4 + [
+            ctypes.POINTER(ctypes.c_size_t)]
+        lib.fa_fwd_schedule_for.restype = ci
         _lib = lib
         return lib
 
@@ -197,6 +200,23 @@ def set_schedule(kind):
     if st != FA_OK:
         raise FAError(st, "fa_set_schedule")
     _ws_cache.clear()
+
+
+def schedule_for(B, Hq, Hkv, Nq, Nkv, D, causal, sms):
+    """``schedule`` for a GPU with ``sms`` SMs, computed on the host without
+    a device (``fa_fwd_schedule_for``); adds ``"workspace"``, the scratch
+    bytes ``fa_fwd_ws`` would need there."""
+    out = [ctypes.c_int(0) for _ in range(4)]
+    ws = ctypes.c_size_t(0)
+    st = int(load().fa_fwd_schedule_for(B, Hq, Hkv, Nq, Nkv, D,
+                                        1 if causal else 0, sms,
+                                        *[ctypes.byref(o) for o in out],
+                                        ctypes.byref(ws)))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_schedule_for")
+    kind, ctas, pieces, bpc = (int(o.value) for o in out)
+    return {"kind": SCHEDULES[kind], "ctas": ctas, "pieces": pieces,
+            "blocks_per_cta": bpc, "workspace": int(ws.value)}
 
 
 def workspace_size(B, Hq, Hkv, Nq, Nkv, D, causal):

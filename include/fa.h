@@ -187,6 +187,18 @@ int fa_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
                     int* blocks_per_cta);
 
 /*
+ * fa_fwd_schedule_for — fa_fwd_schedule for a GPU with `sms` SMs, without
+ * touching any device (the choice depends only on the shape, the SM count
+ * and fa_set_schedule); also writes the scratch fa_fwd_ws would need there
+ * to *workspace.  FA_ERR_INVALID_VALUE for sms < 1 or a NULL output;
+ * other argument errors as fa_fwd_workspace_size.
+ */
+int fa_fwd_schedule_for(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                        int causal, int sms, int* kind, int* ctas,
+                        int* pieces, int* blocks_per_cta,
+                        size_t* workspace);
+
+/*
  * fa_set_schedule — force the schedule of later calls, process-wide, for
  * testing and tuning (the default, FA_SCHEDULE_AUTO, chooses per shape from
  * an estimate of each schedule's time).

@@ -1,0 +1,129 @@
+"""The work schedule the host plans for a shape (fa_fwd_schedule_for: no GPU
+needed).  Checks the choices measured on GB300 (152 SMs), the split-KV and
+stream shapes and their scratch sizes, the forced settings, and invariants
+of every schedule over a grid of shapes and SM counts."""
+
+import itertools
+import math
+
+import pytest
+
+from exact_io_aware_fa2_gb300 import fa
+
+SLOT = {64: 256 * 66 * 4, 128: 256 * 130 * 4}   # stream / two-tile split slot
+
+
+@pytest.fixture(autouse=True)
+def auto_schedule():
+    fa.set_schedule("auto")
+    yield
+    fa.set_schedule("auto")
+
+
+def sched(B, Hq, Hkv, Nq, Nkv, D, causal=False, sms=152):
+    return fa.schedule_for(B, Hq, Hkv, Nq, Nkv, D, causal, sms)
+
+
+@pytest.mark.parametrize("shape,kind", [
+    ((1, 8, 8, 4096, 8192, 128), "plain"),     # 128 pairs: 84% of a wave
+    ((1, 9, 9, 4096, 8192, 128), "plain"),     # 144 pairs
+    ((1, 5, 5, 4096, 8192, 128), "stream"),    # 80 pairs: 53% of a wave
+    ((1, 7, 7, 4096, 8192, 128), "stream"),    # 112 pairs
+    ((1, 25, 25, 2048, 8192, 128), "stream"),  # 200 pairs: 1.3 waves
+    ((1, 5, 5, 4096, 4096, 128), "stream"),    # 80 pairs, 4096 keys
+    ((1, 5, 5, 4096, 2048, 128), "plain"),     # short rows: overhead wins
+    ((1, 5, 5, 4096, 8192, 64), "stream"),
+])
+def test_choices_measured_on_gb300(shape, kind):
+    """The estimate picks the schedule measured faster on GB300 (stream
+    against plain: 74 vs 99 us at 80 pairs, 95 vs 99 at 112, 156 vs 189 at
+    200 pairs, 50 vs 55 with 4096 keys; plain: 99 vs 105 at 128 pairs, 101
+    vs 113 at 144, 33 vs 38 on 2048-key rows)."""
+    assert sched(*shape)["kind"] == kind
+
+
+def test_headline_runs_one_pair_per_cta():
+    s = sched(1, 8, 8, 4096, 8192, 128)
+    assert s == {"kind": "plain", "ctas": 128, "pieces": 1,
+                 "blocks_per_cta": 0, "workspace": 0}
+
+
+def test_decode_shape_splits_packed_gqa():
+    # 32 query heads over 8 kv heads, 128 rows each: packed into 8 heads of
+    # 512 rows = 2 pairs each; 256 K/V blocks cut into 9 pieces.
+    s = sched(1, 32, 8, 128, 32768, 128)
+    assert s["kind"] == "split_kv" and s["pieces"] == 9
+    assert s["ctas"] == 2 * 8 * 9
+    assert s["workspace"] == s["ctas"] * SLOT[128]
+
+
+def test_causal_and_wide_shapes_never_stream():
+    for shape in [(1, 5, 5, 4096, 8192, 128, True),
+                  (1, 5, 5, 4096, 8192, 256, False),
+                  (1, 5, 5, 4096, 8192, 192, False),
+                  (4, 16, 16, 2048, 2048, 64, True)]:
+        assert sched(*shape)["kind"] != "stream"
+        fa.set_schedule("stream")
+        assert sched(*shape)["kind"] != "stream"
+        fa.set_schedule("auto")
+
+
+def test_forced_settings():
+    fa.set_schedule("plain")
+    s = sched(1, 8, 8, 128, 32768, 128)
+    assert s["kind"] == "plain" and s["workspace"] == 0
+    fa.set_schedule("stream")
+    # one block per CTA when there are fewer blocks than SMs: 2 pairs of 24
+    s = sched(1, 2, 2, 256, 3000, 128)
+    assert s["kind"] == "stream" and s["blocks_per_cta"] == 1
+    assert s["ctas"] == 48 and s["workspace"] == 48 * (SLOT[128] + 64)
+    fa.set_schedule("auto")
+    assert sched(1, 2, 2, 256, 3000, 128)["kind"] != "stream"
+
+
+def test_rejects_bad_arguments():
+    with pytest.raises(fa.FAError):
+        sched(1, 8, 8, 4096, 8192, 128, sms=0)
+    with pytest.raises(fa.FAError):
+        sched(1, 8, 3, 4096, 8192, 128)          # Hq % Hkv != 0
+    with pytest.raises(fa.FAError):
+        sched(1, 8, 8, 4096, 8192, 96)           # unsupported head dim
+
+
+SHAPES = list(itertools.product(
+    [1, 3], [1, 8, 24], [1, 4096], [1, 700, 8192], [64, 128, 256],
+    [False, True]))
+
+
+@pytest.mark.parametrize("sms", [8, 76, 152, 160])
+def test_invariants(sms):
+    for B, Hq, Nq, Nkv, D, causal in SHAPES:
+        for Hkv in sorted({1, Hq}):
+            s = sched(B, Hq, Hkv, Nq, Nkv, D, causal, sms)
+            packed = not causal and Hq != Hkv
+            H, N = (Hkv, (Hq // Hkv) * Nq) if packed else (Hq, Nq)
+            one_tile = D in (192, 256) or (D == 64 and causal)
+            rows = 128 if one_tile else 256
+            units = math.ceil(N / rows) * H * B
+            what = (B, Hq, Hkv, Nq, Nkv, D, causal, sms, s)
+            if s["kind"] == "plain":
+                assert s["ctas"] == units and s["pieces"] == 1, what
+                assert s["workspace"] == 0, what
+            elif s["kind"] == "split_kv":
+                keys = 64 if one_tile else 128
+                longest = math.ceil((min(N, Nkv) if causal else Nkv) / keys)
+                assert 2 <= s["pieces"] <= 64, what
+                assert s["pieces"] <= max(1, longest // 4), what
+                assert s["ctas"] == units * s["pieces"], what
+                assert units * 2 <= sms, what
+                slot = (rows * (D + 2)) * 4
+                assert s["workspace"] == units * s["pieces"] * slot, what
+            else:
+                assert not causal and D in (64, 128), what
+                nbp = math.ceil(Nkv / 128)
+                total = units * nbp
+                L = s["blocks_per_cta"]
+                assert L == math.ceil(total / sms), what
+                assert s["ctas"] == math.ceil(total / L) <= sms, what
+                assert 2 * L >= nbp, what
+                assert s["workspace"] == s["ctas"] * (SLOT[D] + 64), what
