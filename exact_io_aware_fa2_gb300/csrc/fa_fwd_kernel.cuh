@@ -22,7 +22,9 @@
 //              tail, keeps the row's reference max m and sum l in the log2
 //              domain (scale folded into one FFMA), writes P = exp2(s*c - m)
 //              as bf16 into TMEM, rescales its O accumulator in TMEM when m
-//              moves, and finally writes O / l and the LSE.
+//              moves, and finally writes O / l and the LSE (each warp stages
+//              its 32 rows in the K ring, idle once the last S MMA has run,
+//              and one lane writes them with TMA stores).
 //   TMA producer: Q_A and Q_B once, then K_j and V_j into two rings of
 //              shared-memory stages (128-byte swizzle).
 //   MMA issuer (one thread), in the order
