@@ -109,6 +109,22 @@ def test_binding_rejects_bad_tensors():
         fa._check(qb.transpose(2, 3), qb, qb)
 
 
+def test_host_binding_rejects_bad_tensors_before_any_device_work():
+    """fa.fwd_host takes CPU bf16 [B, H, N, D] tensors; anything else is
+    rejected on the host before buffers are allocated or the library is
+    called."""
+    import torch
+    qf = torch.zeros(1, 2, 8, 64, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        fa.fwd_host(qf, qf, qf)
+    qb = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    kb = torch.zeros(1, 2, 5, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fwd_host(qb, kb, qb)                  # k and v shapes differ
+    with pytest.raises(ValueError):
+        fa.fwd_host(qb[0], qb[0], qb[0])         # not 4-D
+
+
 def test_noalloc_limit_matches_header():
     text = open(HEADER).read()
     m = re.search(r"#define\s+FA_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)",
