@@ -26,7 +26,11 @@ Sources (titles of the pages this follows):
 
 Parity status: every public function here is pinned by CPU tests against
 closed forms, invariants, a library routine and the brute force; none is
-"parity unpinned".
+"parity unpinned".  ``probabilities_fp64`` is pinned by hand-derived weight
+matrices (tests/golden/closed_forms.json, field "p", including a
+grouped-query case whose kv heads differ) and by P V equalling the output of
+plain multi-head attention on repeated K/V; planted mistakes in its scale,
+head map, normalisation axis and mask fail those pins.
 """
 
 from .attention import (  # noqa: F401

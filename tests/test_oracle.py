@@ -50,6 +50,9 @@ def test_golden_closed_forms(case):
     O, L = oracle.attention_fp64(q, k, v, case["scale"], case["causal"])
     assert torch.allclose(O, o_ref, atol=1e-12, rtol=0)
     assert torch.allclose(L, lse_ref, atol=1e-12, rtol=0)
+    # the probability matrix, against the weights the derivation names
+    P = oracle.probabilities_fp64(q, k, v, case["scale"], case["causal"])
+    assert torch.allclose(P, _t(case["p"]), atol=1e-12, rtol=0)
     # the brute force and both recurrences reach the same closed form
     Ob, Lb = oracle.attention_loops(case["q"], case["k"], case["v"],
                                     case["scale"], case["causal"])
@@ -72,6 +75,29 @@ def test_rows_of_p_sum_to_one(causal):
                           atol=1e-12, rtol=0)
     if causal:  # no weight above the diagonal
         assert torch.all(P.triu(diagonal=1) == 0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2), (6, 1)])
+def test_p_times_v_is_the_output_of_mha_on_repeated_kv(Hq, Hkv, causal):
+    """P from probabilities_fp64, applied to V, gives the output that the
+    (golden-pinned) attention_fp64 computes for plain multi-head attention
+    on K and V repeated per query head: this fixes P's scale, mask and GQA
+    head map together (a wrong one changes the weights of some row)."""
+    q, k, v = _rand(2, Hq, Hkv, 29, 41, 8, 15, std=2.0)
+    g = Hq // Hkv
+    scale = 0.37
+    P = oracle.probabilities_fp64(q, k, v, scale, causal)
+    kr, vr = k.repeat_interleave(g, dim=1), v.repeat_interleave(g, dim=1)
+    O, L = oracle.attention_fp64(q, kr, vr, scale, causal)
+    assert torch.allclose(P @ vr, O, atol=1e-12, rtol=0)
+    # ln of the largest weight of a row is that row's largest score minus
+    # LSE; the scores come from the MHA inputs, not from P
+    S = (q @ kr.transpose(-1, -2)) * oatt.scale_fp64(scale)
+    if causal:
+        S = S.masked_fill(~oatt.visible(torch.arange(29), 41, True), -math.inf)
+    assert torch.allclose(P.max(-1).values.log(),
+                          S.max(-1).values - L, atol=1e-12, rtol=0)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -253,14 +279,43 @@ def test_oracle_on_bf16_inputs_upcasts_exactly():
 # ------------------------------------------------------------ planted mistakes
 
 def _golden_pins_pass():
-    """True iff every golden closed form still holds for attention_fp64."""
+    """True iff every golden closed form still holds for attention_fp64 and
+    probabilities_fp64 (looked up in the module, so a planted mistake in
+    either one is what runs)."""
     for case in _load_golden():
         q, k, v = _t(case["q"]), _t(case["k"]), _t(case["v"])
-        O, L = oracle.attention_fp64(q, k, v, case["scale"], case["causal"])
+        O, L = oatt.attention_fp64(q, k, v, case["scale"], case["causal"])
+        P = oatt.probabilities_fp64(q, k, v, case["scale"], case["causal"])
         if not (torch.allclose(O, _t(case["o"]), atol=1e-9) and
-                torch.allclose(L, _t(case["lse"]), atol=1e-9)):
+                torch.allclose(L, _t(case["lse"]), atol=1e-9) and
+                torch.allclose(P, _t(case["p"]), atol=1e-9)):
             return False
     return True
+
+
+def _probabilities_variant(scale_used, head_map, axis, masked):
+    """probabilities_fp64 with one planted mistake: the scale it applies,
+    the kv head it reads, the axis it normalises over, or the mask."""
+    def fn(q, k, v, scale, causal):
+        B, Hq, Nq, _ = q.shape
+        Hkv, Nkv = k.shape[1], k.shape[2]
+        P = torch.empty(B, Hq, Nq, Nkv, dtype=F64)
+        for b in range(B):
+            for hq in range(Hq):
+                hk = head_map(hq, Hq, Hkv)
+                S = (q[b, hq].double() @ k[b, hk].double().T) * \
+                    scale_used(scale)
+                if masked:
+                    S = S.masked_fill(~oatt.visible(torch.arange(Nq), Nkv,
+                                                    causal), -math.inf)
+                E = torch.exp(S - S.max(dim=axis, keepdim=True).values)
+                P[b, hq] = E / E.sum(dim=axis, keepdim=True)
+        return P
+    return fn
+
+
+_GQA = oatt.kv_head_index
+_SCALE = oatt.scale_fp64
 
 
 def _row_block_no_lse_max(qrows, kh, vh, rows, s64, causal):
@@ -309,11 +364,26 @@ MUTANTS = {
     "lse_without_max": ("_row_block", _row_block_no_lse_max),
     "output_not_normalised": ("_row_block", _row_block_unnormalised),
     "keys_used_as_values": ("_row_block", _row_block_transposed_v),
+    "p_scale_dropped": ("probabilities_fp64", _probabilities_variant(
+        lambda s: 1.0, _GQA, 1, True)),
+    "p_gqa_modulo_mapping": ("probabilities_fp64", _probabilities_variant(
+        _SCALE, lambda hq, Hq, Hkv: hq % Hkv, 1, True)),
+    "p_normalised_over_queries": ("probabilities_fp64", _probabilities_variant(
+        _SCALE, _GQA, 0, True)),
+    "p_mask_dropped": ("probabilities_fp64", _probabilities_variant(
+        _SCALE, _GQA, 1, False)),
 }
 
 
 def test_pins_pass_on_unmodified_oracle():
     assert _golden_pins_pass()
+    # the planted variant without a mistake passes too
+    oracle_p = oatt.probabilities_fp64
+    try:
+        oatt.probabilities_fp64 = _probabilities_variant(_SCALE, _GQA, 1, True)
+        assert _golden_pins_pass()
+    finally:
+        oatt.probabilities_fp64 = oracle_p
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
