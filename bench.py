@@ -23,7 +23,11 @@ samples of the same workload: one 128-row query tile per step.
 
 The line's ``sdpa`` object times torch's scaled_dot_product_attention
 (cuDNN, flash and memory-efficient backends, each alone) on the same inputs
-and in the same way, for comparison (``--no-sdpa`` skips it).
+and in the same way, for comparison (``--no-sdpa`` skips it).  Its
+``configs`` object times each of the five workloads the metric is specified
+on (tiny, the pages' shape, causal D64, causal GQA, long causal with large
+logits) in this process with the same steps, warm-up and L2 flush
+(``--no-configs`` skips it); ``value`` stays the chosen workload's.
 """
 
 import argparse
@@ -61,7 +65,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-sdpa", action="store_true",
                     help="skip the torch SDPA comparison column")
-    ap.add_argument("--sdpa-steps", type=int, default=200)
+    ap.add_argument("--sdpa-steps", type=int, default=None,
+                    help="steps of each SDPA backend (default: --steps)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the five specification workloads")
     return ap.parse_args()
 
 
@@ -224,6 +231,26 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True,
+                             timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
 def cpu_baseline(w, q, k, v, seconds):
     """The oracle as it stands, on this host's cores, over (batch, head)
     slices of the workload (repeating the workload if it is short) until
@@ -246,7 +273,7 @@ def cpu_baseline(w, q, k, v, seconds):
     dt = time.perf_counter() - t0
     flops = w.flops / len(slices) * done
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores,
-            "kind": "oracle",
+            "cpu_model": cpu_model(), "kind": "oracle",
             "sample": f"{done} (batch, head) slices of {w.name} "
                       f"({len(slices)} per workload), float64, {dt:.1f} s"}
 
@@ -291,7 +318,7 @@ def run_reference(args, w):
         "config": {"workload": w.name, **w.as_dict(),
                    "sample": "one 128-row query tile per step"},
         "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores,
-                         "kind": "oracle",
+                         "cpu_model": cpu_model(), "kind": "oracle",
                          "sample": "one 128-row query tile of the workload "
                                    "per step, float64"},
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -305,8 +332,9 @@ SDPA_BACKENDS = ("CUDNN_ATTENTION", "FLASH_ATTENTION", "EFFICIENT_ATTENTION")
 
 def sdpa_column(w, q, k, v, o_ours, flush, stream, steps, warmup=5):
     """torch's scaled_dot_product_attention on the same resident inputs, one
-    backend at a time, timed like our kernel (L2 flushed before each step,
-    CUDA events on the launching stream).  A comparison, not part of the
+    backend at a time, timed exactly like our kernel (time_steps: the same
+    step and warm-up counts, L2 flushed before each step, CUDA events on the
+    launching stream).  A comparison, not part of the
     path.  Grouped-query shapes use SDPA's own GQA support; a backend that
     lacks it gets K/V expanded to every query head beforehand (untimed),
     which the entry notes.  Returns {backend: {...}} with TFLOPS and the
@@ -335,22 +363,15 @@ def sdpa_column(w, q, k, v, o_ours, flush, stream, steps, warmup=5):
                     gqa = False
                     entry["note"] = "K/V expanded to Hq heads (untimed)"
                     res = step()
-                for _ in range(warmup):
-                    step()
+                starts, ends = time_steps(step, flush, stream, steps,
+                                          warmup, torch.cuda.synchronize)
                 torch.cuda.synchronize()
-                ev = [(torch.cuda.Event(enable_timing=True),
-                       torch.cuda.Event(enable_timing=True))
-                      for _ in range(steps)]
-                for i, (s, e) in enumerate(ev):
-                    flush.fill_(float(i))
-                    s.record(stream)
-                    step()
-                    e.record(stream)
-                torch.cuda.synchronize()
-            ms = sum(s.elapsed_time(e) for s, e in ev) / steps
+            per = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+            ms = sum(per) / steps
             entry.update({
                 "value": w.flops / (ms * 1e-3) / 1e12, "unit": UNIT,
-                "ms_per_step": ms, "steps": steps,
+                "ms_per_step": ms, "ms_per_step_median":
+                    statistics.median(per), "steps": steps,
                 "max_abs_diff_vs_ours":
                     float((res.float() - o_ours.float()).abs().max())})
         except Exception as exc:  # a backend this GPU/torch cannot run
@@ -364,6 +385,77 @@ def sdpa_column(w, q, k, v, o_ours, flush, stream, steps, warmup=5):
     return out
 
 
+# The five workloads the metric is specified on (tiny, the pages' shape,
+# causal D64, causal GQA, long causal with large logits), each timed in the
+# bench process the same way as the headline and reported in ``configs``.
+SPEC_WORKLOADS = ("tiny_128_d64", "pages_b1_h8_q4096_kv8192_d128",
+                  "causal_b4_h16_n2048_d64",
+                  "causal_gqa_b2_hq32_hkv8_n8192_d128",
+                  "causal_b1_h16_n32768_d128_large_logits")
+
+
+def time_steps(launch, flush, stream, steps, warmup, barrier):
+    """CUDA-event pairs around each of ``steps`` calls of ``launch``, after
+    ``warmup`` (at least 3) untimed ones and a barrier.  L2 is flushed (a
+    512 MiB write) before every call, outside its event pair; events are
+    recorded on the launching stream.  Before the first timed call a few
+    flushes are queued, so the host runs ahead of the GPU and no step's
+    events include host launch time.  Returns (starts, ends); the caller
+    synchronises (barrier) after."""
+    for i in range(max(3, warmup)):
+        flush.fill_(float(i))
+        launch()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier()
+    for i in range(4):
+        flush.fill_(float(-i))
+    for i in range(steps):
+        flush.fill_(float(i))                        # evict L2 (untimed)
+        starts[i].record(stream)
+        launch()
+        ends[i].record(stream)
+    return starts, ends
+
+
+def spec_configs(args, fa, flush, stream, dev, headline):
+    """Every workload of SPEC_WORKLOADS timed like the headline (same steps,
+    warm-up, L2 flush and events) in this process: TFLOPS from the mean
+    step, the median step, and the fraction of the bf16 peak."""
+    peak, _ = peaks()
+    out = {}
+    for name in SPEC_WORKLOADS:
+        w = WORKLOADS[name]
+        q, k, v = (t.to(dev) for t in make_inputs(w))
+        o = torch.empty_like(q)
+        lse = torch.empty(w.B, w.Hq, w.Nq, dtype=torch.float32, device=dev)
+
+        def launch():
+            fa.fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse)
+
+        def sync():
+            torch.cuda.synchronize(dev)
+        starts, ends = time_steps(launch, flush, stream, args.steps,
+                                  args.warmup, sync)
+        sync()
+        if fa.last_device_error() != 0:
+            raise RuntimeError(f"bounded-wait timeout timing {name}")
+        per = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        mean, med = sum(per) / len(per), statistics.median(per)
+        tf = w.flops / (mean * 1e-3) / 1e12
+        out[name] = {
+            "value": tf, "unit": UNIT, "ms_per_step": mean,
+            "ms_per_step_median": med,
+            "value_at_median": w.flops / (med * 1e-3) / 1e12,
+            "frac": tf / peak, "steps": args.steps,
+            "kernel": kernel_for(w),
+            "schedule": fa.schedule(w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D,
+                                    w.causal),
+            "headline": name == headline.name}
+        del q, k, v, o, lse
+    return out
+
+
 def run_ours(args, w):
     from exact_io_aware_fa2_gb300 import fa
     ws, rank, local = dist_env()
@@ -374,6 +466,11 @@ def run_ours(args, w):
     dev = torch.device("cuda", local if ws > 1 else 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
 
     q_h, k_h, v_h = make_inputs(w)
     q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
@@ -392,37 +489,29 @@ def run_ours(args, w):
         else:
             fa.fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse)
 
-    for _ in range(max(3, args.warmup)):
-        launch()
+    launch()
     torch.cuda.synchronize(dev)
     if fa.last_device_error() != 0:
-        raise RuntimeError("bounded-wait timeout during warm-up")
-
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-
-    def barrier():
-        if ws > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize(dev)
+        raise RuntimeError("bounded-wait timeout in the first call")
 
     smi_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(dev.index))
                     .split(",")[dev.index]) if os.environ.get(
         "CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else dev.index
     with ClockSampler(smi_index) as clk:
+        # the sampler starts first; the warm-up steps run after its start-up
         time.sleep(0.3)
         barrier()
         wall0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.fill_(float(i))                    # evict L2 (untimed)
-            starts[i].record(stream)
-            launch()
-            ends[i].record(stream)
+        starts, ends = time_steps(launch, flush, stream, args.steps,
+                                  args.warmup, barrier)
         barrier()
         wall = time.perf_counter() - wall0
-    if fa.last_device_error() != 0:
-        raise RuntimeError("bounded-wait timeout during the timed loop")
-    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        if fa.last_device_error() != 0:
+            raise RuntimeError("bounded-wait timeout during the timed loop")
+        per = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+        configs = None
+        if ws == 1 and not args.no_configs:
+            configs = spec_configs(args, fa, flush, stream, dev, w)
     ms = sum(per) / len(per)
     ms_max = max_over_ranks(ms, dev)
     value = job_tflops(w.flops, ms_max, ws)
@@ -484,7 +573,8 @@ def run_ours(args, w):
 
     sdpa = None
     if ws == 1 and not args.no_sdpa:
-        sdpa = sdpa_column(w, q, k, v, o, flush, stream, args.sdpa_steps)
+        sdpa = sdpa_column(w, q, k, v, o, flush, stream,
+                           args.sdpa_steps or args.steps, args.warmup)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -530,6 +620,8 @@ def run_ours(args, w):
         "wall_s_timed_loop": wall,
         "ms_per_step_min": min(per), "ms_per_step_median":
             statistics.median(per),
+        "ms_per_step_all": per,
+        "configs": configs,
     }
     print(json.dumps(line), flush=True)
 

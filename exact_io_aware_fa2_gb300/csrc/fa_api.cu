@@ -99,6 +99,22 @@ int* g_status_word[kMaxDevices];
 int g_sm_count[kMaxDevices];
 cudaMemPool_t g_pool[kMaxDevices];
 
+// Split-KV scratch for fa_fwd_noalloc: a fixed array in device memory, part
+// of the loaded module, so that entry point never allocates.  Each device
+// that loads the library holds it until the process exits.  In host code
+// the name only stands for the symbol; its device address comes from
+// cudaGetSymbolAddress, taken once per device in device_ready.
+static __device__ __align__(256) unsigned char
+    g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+void* g_noalloc_ptr[kMaxDevices];   // nullptr if the lookup failed
+
+// Freed split-KV / stream scratch the pool keeps reserved for later calls.
+// Every shape needs at most about 30 MB on a 152-SM GB300 (the need grows
+// with the SM count, not the sequence lengths), so this keeps one call's
+// scratch; anything above it returns to the device at the next
+// synchronisation.
+constexpr uint64_t kPoolKeepBytes = 64ull << 20;
+
 // Per-device readiness: compute capability 10.3, the kernels' shared memory
 // opt-in and the device address of the status word, done once per device
 // with that device current.
@@ -116,6 +132,7 @@ int device_ready(int** word_out, int* dev_out = nullptr) {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor,
                                dev) != cudaSuccess) {
       status[dev] = FA_ERR_CUDA;
+      cudaGetLastError();
       return;
     }
     if (major != 10 || minor != 3) {
@@ -138,29 +155,41 @@ int device_ready(int** word_out, int* dev_out = nullptr) {
         opt_in_smem_wide<256, false>() != cudaSuccess ||
         opt_in_smem_wide<256, true>() != cudaSuccess) {
       status[dev] = FA_ERR_CUDA;
+      cudaGetLastError();
       return;
     }
     void* word = nullptr;
     if (cudaGetSymbolAddress(&word, fa::g_fa_status) != cudaSuccess) {
       status[dev] = FA_ERR_CUDA;
+      cudaGetLastError();   // leave no pending error for the next launch
       return;
     }
+    void* scratch = nullptr;
+    if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) == cudaSuccess)
+      g_noalloc_ptr[dev] = scratch;
+    else
+      cudaGetLastError();   // only fa_fwd_noalloc fails then
     g_status_word[dev] = static_cast<int*>(word);
     if (cudaDeviceGetAttribute(&g_sm_count[dev],
                                cudaDevAttrMultiProcessorCount,
-                               dev) != cudaSuccess)
+                               dev) != cudaSuccess) {
+      cudaGetLastError();
       return;
+    }
     // Stream-ordered pool for fa_fwd's split-KV scratch (fa_fwd_ws takes
-    // the caller's memory instead); freed blocks stay cached in the pool.
+    // the caller's memory instead); up to kPoolKeepBytes of freed blocks
+    // stay reserved for the next call.
     cudaMemPoolProps props = {};
     props.allocType = cudaMemAllocationTypePinned;
     props.location.type = cudaMemLocationTypeDevice;
     props.location.id = dev;
-    uint64_t keep = ~0ull;
+    uint64_t keep = kPoolKeepBytes;
     if (cudaMemPoolCreate(&g_pool[dev], &props) != cudaSuccess ||
         cudaMemPoolSetAttribute(g_pool[dev], cudaMemPoolAttrReleaseThreshold,
-                                &keep) != cudaSuccess)
+                                &keep) != cudaSuccess) {
+      cudaGetLastError();
       return;
+    }
     status[dev] = FA_OK;
   });
   if (status[dev] == FA_OK && word_out != nullptr) *word_out = g_status_word[dev];
@@ -289,7 +318,7 @@ RunShape run_shape(int Hq, int Hkv, int Nq, int causal) {
   return {Hkv, static_cast<int>(packed)};
 }
 
-// Scratch: for split-KV one fp32 slot of unit_rows(D) * (D + 2) words per
+// Scratch: for split-KV one fp32 slot of unit_rows(D) * (D + 3) words per
 // (batch, head, unit of query rows, K/V range); for the stream schedule one
 // slot per CTA plus its flags.
 int64_t workspace_bytes(int B, int Hq, int Nq, int D, int causal,
@@ -301,15 +330,65 @@ int64_t workspace_bytes(int B, int Hq, int Nq, int D, int causal,
   if (splits <= 1) return 0;
   const int64_t rows_u = unit_rows(D, causal);
   const int64_t units = (Nq + rows_u - 1) / rows_u;
-  const int64_t slot = rows_u * (D + 2);
+  const int64_t slot = rows_u * (D + 3);
   return static_cast<int64_t>(B) * Hq * units * splits * slot * 4;
+}
+
+// Tensor maps are cached per (pointer, [BH, N, D] extent, box, element
+// type): a map holds only an address, extents, strides and the box, so an
+// entry stays valid for any later tensor at that address with that shape.
+// A small least-recently-used table, shared by all threads and devices.
+struct MapKey {
+  const void* ptr;
+  long long BH;
+  int N, D, box_rows, e4m3;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && BH == o.BH && N == o.N && D == o.D &&
+           box_rows == o.box_rows && e4m3 == o.e4m3;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  uint64_t last_use;   // 0: empty
+};
+constexpr int kMapCacheEntries = 64;
+MapEntry g_map_cache[kMapCacheEntries];
+uint64_t g_map_clock = 0;
+std::mutex g_map_mu;
+std::atomic<size_t> g_map_encodes{0};
+
+// Looks the key up; on a miss calls `encode` to fill a free or the least
+// recently used entry.  Returns FA_OK or the encoder's error.
+template <typename Encode>
+int cached_map(CUtensorMap* out, const MapKey& key, Encode encode) {
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  MapEntry* victim = &g_map_cache[0];
+  for (MapEntry& e : g_map_cache) {
+    if (e.last_use != 0 && e.key == key) {
+      e.last_use = ++g_map_clock;
+      *out = e.map;
+      return FA_OK;
+    }
+    if (e.last_use < victim->last_use) victim = &e;
+  }
+  const int st = encode(&victim->map);
+  g_map_encodes.fetch_add(1, std::memory_order_relaxed);
+  if (st != FA_OK) {
+    victim->last_use = 0;
+    return st;
+  }
+  victim->key = key;
+  victim->last_use = ++g_map_clock;
+  *out = victim->map;
+  return FA_OK;
 }
 
 // Tensor map of a contiguous bf16 [BH, N, D] tensor, read in boxes of 64
 // head-dim elements (one 128-byte swizzle row) by `box_rows` sequence rows,
 // with the 128-byte swizzle.  Rows past N are zero-filled by the TMA unit.
-int encode_bhnd(CUtensorMap* map, const void* ptr, long long BH, int N,
-                int D, int box_rows = fa::kBM) {
+int encode_bhnd_uncached(CUtensorMap* map, const void* ptr, long long BH,
+                         int N, int D, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return FA_ERR_CUDA;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D),
@@ -328,10 +407,18 @@ int encode_bhnd(CUtensorMap* map, const void* ptr, long long BH, int N,
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+int encode_bhnd(CUtensorMap* map, const void* ptr, long long BH, int N,
+                int D, int box_rows = fa::kBM) {
+  return cached_map(map, MapKey{ptr, BH, N, D, box_rows, 0},
+                    [&](CUtensorMap* m) {
+                      return encode_bhnd_uncached(m, ptr, BH, N, D, box_rows);
+                    });
+}
+
 // The same for a one-byte (e4m3) [BH, N, D] tensor: boxes of 128 head-dim
 // elements (one 128-byte swizzle row) by 128 sequence rows.
-int encode_bhnd_e4m3(CUtensorMap* map, const void* ptr, long long BH, int N,
-                     int D) {
+int encode_bhnd_e4m3_uncached(CUtensorMap* map, const void* ptr, long long BH,
+                              int N, int D) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return FA_ERR_CUDA;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D),
@@ -347,6 +434,14 @@ int encode_bhnd_e4m3(CUtensorMap* map, const void* ptr, long long BH, int N,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+int encode_bhnd_e4m3(CUtensorMap* map, const void* ptr, long long BH, int N,
+                     int D) {
+  return cached_map(map, MapKey{ptr, BH, N, D, fa::kBM, 1},
+                    [&](CUtensorMap* m) {
+                      return encode_bhnd_e4m3_uncached(m, ptr, BH, N, D);
+                    });
 }
 
 // fa_merge_kernel over units of ROWS query rows.
@@ -700,35 +795,6 @@ int fa_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
 
 namespace {
 
-// Split-KV scratch for fa_fwd_noalloc: a fixed array in device memory, part
-// of the loaded module, so that entry point never allocates.  Each device
-// that loads the library holds it until the process exits.  In host code
-// the name only stands for the symbol; its device address comes from
-// cudaGetSymbolAddress.
-static __device__ __align__(256) unsigned char
-    g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
-
-void* g_noalloc_ptr[kMaxDevices];
-
-// Device address of the array on the current device, looked up once per
-// device (with that device current).
-int noalloc_scratch(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
-  static std::once_flag flags[kMaxDevices];
-  static int status[kMaxDevices];
-  std::call_once(flags[dev], [dev] {
-    void* ptr = nullptr;
-    status[dev] = cudaGetSymbolAddress(&ptr, g_noalloc_scratch) == cudaSuccess
-                      ? FA_OK
-                      : FA_ERR_CUDA;
-    g_noalloc_ptr[dev] = ptr;
-  });
-  if (status[dev] == FA_OK) *out = g_noalloc_ptr[dev];
-  return status[dev];
-}
-
 // fa_fwd_host: per-device side streams (host-to-device and device-to-host
 // copies) and events, created once; a mutex per device keeps concurrent
 // callers' enqueue sequences from interleaving on them.  Chunk count
@@ -791,8 +857,14 @@ int fa_fwd_host(const void* q_host, const void* k_host, const void* v_host,
   // forward of its own with B = groups, Hq = Hq / Hkv, Hkv = 1.
   const int64_t groups = static_cast<int64_t>(B) * Hkv;
   const int G = Hq / Hkv;
-  const int n_chunks =
-      static_cast<int>(groups < kHostChunks ? groups : kHostChunks);
+  // At most kHostChunks chunks, more only when a chunk's group count would
+  // pass the grid's batch limit (each chunk runs with B = its groups); the
+  // chunks then take the events round-robin (each event is waited on before
+  // it is recorded again).
+  const int64_t min_chunks = (groups + 65534) / 65535;
+  const int n_chunks = static_cast<int>(
+      min_chunks > kHostChunks ? min_chunks
+                               : (groups < kHostChunks ? groups : kHostChunks));
   const int64_t q_group = static_cast<int64_t>(G) * Nq * D * 2;   // bytes
   const int64_t kv_group = static_cast<int64_t>(Nkv) * D * 2;
   const int64_t lse_group = static_cast<int64_t>(G) * Nq * 4;
@@ -830,8 +902,8 @@ int fa_fwd_host(const void* q_host, const void* k_host, const void* v_host,
         !ok(cudaMemcpyAsync(mptr(q_dev, g0 * q_group),
                             cptr(q_host, g0 * q_group), ng * q_group, h2d,
                             hp.h2d)) ||
-        !ok(cudaEventRecord(hp.in[c], hp.h2d)) ||
-        !ok(cudaStreamWaitEvent(s, hp.in[c], 0)))
+        !ok(cudaEventRecord(hp.in[c % kHostChunks], hp.h2d)) ||
+        !ok(cudaStreamWaitEvent(s, hp.in[c % kHostChunks], 0)))
       return join(FA_ERR_CUDA);
     // compute on the caller's stream
     st = run_forward(cptr(q_dev, g0 * q_group), cptr(k_dev, g0 * kv_group),
@@ -843,8 +915,8 @@ int fa_fwd_host(const void* q_host, const void* k_host, const void* v_host,
                      nullptr, 0, true, s);
     if (st != FA_OK) return join(st);
     // out: this chunk's O and LSE while later chunks copy in and compute
-    if (!ok(cudaEventRecord(hp.done[c], s)) ||
-        !ok(cudaStreamWaitEvent(hp.d2h, hp.done[c], 0)) ||
+    if (!ok(cudaEventRecord(hp.done[c % kHostChunks], s)) ||
+        !ok(cudaStreamWaitEvent(hp.d2h, hp.done[c % kHostChunks], 0)) ||
         !ok(cudaMemcpyAsync(mptr(o_host, g0 * q_group),
                             cptr(o_dev, g0 * q_group), ng * q_group,
                             cudaMemcpyDeviceToHost, hp.d2h)))
@@ -867,7 +939,12 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o,
   if (st != FA_OK) return st;
   if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_INVALID_VALUE;
   void* scratch = nullptr;
-  if (need > 0 && (st = noalloc_scratch(&scratch)) != FA_OK) return st;
+  if (need > 0) {
+    int dev = 0;
+    if ((st = device_ready(nullptr, &dev)) != FA_OK) return st;
+    scratch = g_noalloc_ptr[dev];
+    if (scratch == nullptr) return FA_ERR_CUDA;
+  }
   return fa_fwd_ws(q, k, v, o, lse, B, Hq, Hkv, Nq, Nkv, D, scale, causal,
                    scratch, need, stream);
 }
@@ -917,5 +994,9 @@ int fa_probe_flag_wait(long long timeout_ns, void* stream) {
 }
 
 int fa_version(void) { return 100; }
+
+size_t fa_tensor_map_encodes(void) {
+  return g_map_encodes.load(std::memory_order_relaxed);
+}
 
 }  // extern "C"

@@ -106,9 +106,10 @@ struct FwdCfg {
                                           : idesc_bf16_f32(kBM, kBN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);
   // fp32 words of one partial slot: O rows [256][D] (unnormalised, relative
-  // to the slot's reference max), then m[256] (log2 domain), then l[256].
+  // to the slot's reference max), then m[256] (log2 domain), l[256] (exact
+  // row sums) and w[256] (row sums of the bf16 weights).
   static constexpr int64_t kSlotFloats =
-      static_cast<int64_t>(kTilesPerCta * kBM) * (D + 2);
+      static_cast<int64_t>(kTilesPerCta * kBM) * (D + 3);
 };
 
 // The K ring holds the staged output rows of all eight softmax warps
@@ -191,13 +192,54 @@ __device__ __forceinline__ int kv_blocks(int row0, int Nkv) {
   return (end + kBN - 1) / kBN;
 }
 
+// P = exp2(s * c - m) for the N scores of one row (sr, fp32 bit patterns),
+// packed to bf16x2 into pp (N / 2 words), with two row sums: `exact` of the
+// fp32 values (for the LSE) and `rounded` of the bf16 values, the weights
+// the P V product applies (O is divided by this one, so O / sum is a convex
+// combination of V rows and the rounding of P largely cancels in it).  With
+// MASK, only the first n_vis keys count (the others get p = 0).  The scores
+// are scaled and shifted by one f32x2 FMA per pair, exp2 runs on the MUFU.
+template <int N, bool MASK>
+__device__ __forceinline__ void exp_pack_row(const uint32_t* sr, float c,
+                                             float m_use, int n_vis,
+                                             uint32_t* pp, float& exact,
+                                             float& rounded) {
+  const uint64_t c2 = f2(c, c);
+  const uint64_t nm2 = f2(-m_use, -m_use);
+  uint64_t acc[2] = {0, 0};
+  float r[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    float x0, x1;
+    f2_split(fma2(f2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])),
+                  c2, nm2),
+             x0, x1);
+    if (MASK) {
+      x0 = (i < n_vis) ? x0 : -INFINITY;
+      x1 = (i + 1 < n_vis) ? x1 : -INFINITY;
+    }
+    const float e0 = ex2_approx(x0);
+    const float e1 = ex2_approx(x1);
+    const uint32_t pk = pack_bf16x2(e0, e1);
+    pp[i / 2] = pk;
+    acc[(i >> 1) & 1] = add2(acc[(i >> 1) & 1], f2(e0, e1));
+    const int q = ((i >> 1) & 1) * 2;
+    add_bf16x2_to(r[q], r[q + 1], pk);
+  }
+  float s0, s1;
+  f2_split(add2(acc[0], acc[1]), s0, s1);
+  exact = s0 + s1;
+  rounded = (r[0] + r[1]) + (r[2] + r[3]);
+}
+
 // One K/V block of the online softmax, for the query row this thread owns
 // (TMEM lane = row): reads the block's scores from TMEM at s_addr, takes the
 // row's extreme over the visible keys, moves the reference max m_ref (log2
 // domain) only when the block exceeds it by more than kRescaleLog2, writes
-// P = exp2(s * c - m_ref) as packed bf16 to p_addr, adds the row sum to
-// l_run, and rescales O (at o_addr) when the reference moved and O already
-// holds earlier blocks (`o_live`).  Returns once its TMEM stores are done and
+// P = exp2(s * c - m_ref) as packed bf16 to p_addr, adds the row sums to
+// l_run (exact values) and w_run (the bf16 values; see exp_pack_row), and
+// rescales O (at o_addr) when the reference moved and O already holds
+// earlier blocks (`o_live`).  Returns once its TMEM stores are done and
 // fenced; the caller then signals that P is ready.  Keys from col0 on are
 // visible up to Nkv and, when CAUSAL, up to the row's own index q_abs.
 // Steps: "Hacker News Digest — gpu-computing", section "v1 — базовая
@@ -207,7 +249,7 @@ template <int D, bool CAUSAL>
 __device__ __forceinline__ void softmax_block(
     uint32_t s_addr, uint32_t p_addr, uint32_t o_addr, int col0, int my_row0,
     int q_abs, int Nkv, float c, bool neg_scale, bool o_live, float& m_ref,
-    float& l_run) {
+    float& l_run, float& w_run) {
   uint32_t sr[kBN];
   const bool need_mask =
       (col0 + kBN > Nkv) || (CAUSAL && col0 + kBN - 1 > my_row0);
@@ -273,49 +315,16 @@ __device__ __forceinline__ void softmax_block(
       (move && m_ref != -INFINITY) ? ex2_approx(m_ref - m_new) : 1.f;
   const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
 
-  // ---- P = exp2(s * c - m), row sum, pack to bf16 ----
+  // ---- P = exp2(s * c - m), packed to bf16, both row sums ----
   uint32_t pp[kBN / 2];
-  float rsum;
-  if (!need_mask) {
-    // x = s*c - m on packed pairs (f32x2 FMA), exp2 on the MUFU, packed
-    // row sums, bf16x2 packing of P.
-    const uint64_t c2 = f2(c, c);
-    const uint64_t nm2 = f2(-m_use, -m_use);
-    uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll
-    for (int i = 0; i < kBN; i += 2) {
-      float x0, x1;
-      f2_split(fma2(f2(S_(i), S_(i + 1)), c2, nm2), x0, x1);
-      const float e0 = ex2_approx(x0);
-      const float e1 = ex2_approx(x1);
-      acc[(i >> 1) & 3] = add2(acc[(i >> 1) & 3], f2(e0, e1));
-      pp[i / 2] = pack_bf16x2(e0, e1);
-    }
-    float s0, s1;
-    f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), s0, s1);
-    rsum = s0 + s1;
-  } else {
-    // the same packed loop; invisible keys get x = -inf, so p = 0
-    const uint64_t c2 = f2(c, c);
-    const uint64_t nm2 = f2(-m_use, -m_use);
-    uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll
-    for (int i = 0; i < kBN; i += 2) {
-      float x0, x1;
-      f2_split(fma2(f2(S_(i), S_(i + 1)), c2, nm2), x0, x1);
-      x0 = (i < n_vis) ? x0 : -INFINITY;
-      x1 = (i + 1 < n_vis) ? x1 : -INFINITY;
-      const float e0 = ex2_approx(x0);
-      const float e1 = ex2_approx(x1);
-      acc[(i >> 1) & 3] = add2(acc[(i >> 1) & 3], f2(e0, e1));
-      pp[i / 2] = pack_bf16x2(e0, e1);
-    }
-    float s0, s1;
-    f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), s0, s1);
-    rsum = s0 + s1;
-  }
+  float rsum, wsum;
+  if (!need_mask)
+    exp_pack_row<kBN, false>(sr, c, m_use, kBN, pp, rsum, wsum);
+  else
+    exp_pack_row<kBN, true>(sr, c, m_use, n_vis, pp, rsum, wsum);
 #undef S_
   l_run = l_run * alpha + rsum;
+  w_run = w_run * alpha + wsum;
   m_ref = m_new;
 
   // ---- rescale O when the reference max moved.  S(j) complete means
@@ -399,17 +408,18 @@ __device__ __forceinline__ void flush_rows(const OutRows& out, int lane) {
 }
 
 // The last step for one query row: O (unnormalised, in TMEM at o_addr,
-// relative to the reference max m_ref) divided by the row sum l_run, rounded
-// to bf16 and stored (see OutRows; orow is the row's address for direct
-// stores); LSE = (m_ref + log2 l_run) ln 2 at lse_at (skipped when null).
-// Rows past the end (`in_range` false) store nothing.
+// relative to the reference max m_ref) divided by w_run, the row sum of the
+// bf16 weights P V applied, rounded to bf16 and stored (see OutRows; orow is
+// the row's address for direct stores); LSE = (m_ref + log2 l_run) ln 2 from
+// the exact row sum, at lse_at (skipped when null).  Rows past the end
+// (`in_range` false) store nothing.
 template <int D>
 __device__ __forceinline__ void store_final_row(uint32_t o_addr, float m_ref,
-                                                float l_run,
+                                                float l_run, float w_run,
                                                 __nv_bfloat16* orow,
                                                 float* lse_at, bool in_range,
                                                 const OutRows& out) {
-  const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+  const float inv_l = (w_run > 0.f) ? 1.f / w_run : 0.f;
   const int lane = static_cast<int>(threadIdx.x & 31);
 #pragma unroll
   for (int cc = 0; cc < D / 32; ++cc) {
@@ -629,6 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q_abs = my_row0 + (warp & 3) * 32 + lane;
     float m_ref = -INFINITY;   // reference max (log2 domain) of p and l
     float l_run = 0.f;         // sum of exp2(s*c - m_ref) over seen keys
+    float w_run = 0.f;         // the same sum of the bf16-rounded values
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
       // Warp-uniform outcome: the tcgen05 loads below are .sync.aligned.
@@ -640,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                tmem + lane_off + C::col_p(x),
                                tmem + lane_off + C::col_o(x), (j0 + j) * kBN,
                                my_row0, q_abs, p.Nkv, c, neg_scale, j >= 1,
-                               m_ref, l_run);
+                               m_ref, l_run, w_run);
       __syncwarp();
       if (lane == 0) mbar_arrive(bPFull(x));
     }
@@ -681,6 +692,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       slot[kTilesPerCta * kBM * D + prow] = nb > 0 ? m_ref : -INFINITY;
       slot[kTilesPerCta * kBM * D + kTilesPerCta * kBM + prow] =
           nb > 0 ? l_run : 0.f;
+      slot[kTilesPerCta * kBM * D + 2 * kTilesPerCta * kBM + prow] =
+          nb > 0 ? w_run : 0.f;
     } else {
     if (ok && nb > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(bOFinal, 0, wc));
@@ -695,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int role = warp - kSoftmaxWarp0;
       const OutRows out{sK + static_cast<uint32_t>(role) * (32u * D * 2u),
                         &tmO, my_row0 + (warp & 3) * 32, b * p.Hq + hq, p.Nq};
-      store_final_row<D>(tmem + lane_off + C::col_o(x), m_ref, l_run,
+      store_final_row<D>(tmem + lane_off + C::col_o(x), m_ref, l_run, w_run,
                          p.o + row_idx * D,
                          p.lse != nullptr ? p.lse + row_idx : nullptr,
                          q_abs < p.Nq, out);
@@ -713,13 +726,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Split-KV merge: for every query row, combine the partials of its K/V
 // ranges.  Range s left O_s (unnormalised, relative to its reference max
-// m_s, log2 domain) and l_s; with m = max_s m_s
-//     l = sum_s l_s 2^(m_s - m),   O = sum_s O_s 2^(m_s - m) / l,
-//     LSE = (m + log2 l) ln 2,
+// m_s, log2 domain), l_s (exact row sum) and w_s (row sum of the bf16
+// weights); with m = max_s m_s
+//     l = sum_s l_s 2^(m_s - m),   w = sum_s w_s 2^(m_s - m),
+//     O = sum_s O_s 2^(m_s - m) / w,   LSE = (m + log2 l) ln 2,
 // the same rescaling the online softmax applies between K/V blocks.  A
 // partial slot covers one unit of ROWS query rows (a tile pair of the
 // two-tile kernel, a tile of the wide-head kernel): fp32 O [ROWS][D], then
-// m [ROWS], then l [ROWS].  One thread per (row, 4 columns).
+// m [ROWS], l [ROWS], w [ROWS].  One thread per (row, 4 columns).
 template <int D>
 struct MergeCfg {
   static constexpr int kChunks = D / 4;           // float4 per row
@@ -731,7 +745,7 @@ template <int D, int ROWS>
 __global__ void __launch_bounds__(MergeCfg<D>::kThreads)
     fa_merge_kernel(const __grid_constant__ FwdParams p) {
   using M = MergeCfg<D>;
-  constexpr int64_t kSlot = static_cast<int64_t>(ROWS) * (D + 2);
+  constexpr int64_t kSlot = static_cast<int64_t>(ROWS) * (D + 3);
   const int splits = p.kv_splits;
   constexpr int kBlocksPerUnit = ROWS / M::kRowsPerBlock;
   const int unit = static_cast<int>(blockIdx.x) / kBlocksPerUnit;
@@ -750,7 +764,7 @@ __global__ void __launch_bounds__(MergeCfg<D>::kThreads)
   float m = -INFINITY;
   for (int s = 0; s < splits; ++s)
     m = fmaxf(m, base[s * kSlot + ROWS * D + prow]);
-  float l = 0.f;
+  float l = 0.f, wsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
   for (int s = 0; s < splits; ++s) {
@@ -759,13 +773,14 @@ __global__ void __launch_bounds__(MergeCfg<D>::kThreads)
     if (ms == -INFINITY) continue;                // range saw no key
     const float w = ex2_approx(ms - m);
     l += slot[ROWS * D + ROWS + prow] * w;
+    wsum += slot[ROWS * D + 2 * ROWS + prow] * w;
     const float4 o = reinterpret_cast<const float4*>(slot + prow * D)[ch];
     acc.x += o.x * w;
     acc.y += o.y * w;
     acc.z += o.z * w;
     acc.w += o.w * w;
   }
-  const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+  const float inv_l = (wsum > 0.f) ? 1.f / wsum : 0.f;
   const size_t row_idx =
       (static_cast<size_t>(b) * p.Hq + hq) * static_cast<size_t>(p.Nq) +
       static_cast<size_t>(q_row);

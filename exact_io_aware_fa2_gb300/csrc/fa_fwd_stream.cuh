@@ -115,10 +115,11 @@ __device__ __forceinline__ StreamSeg stream_segment(const FwdParams& p,
 
 // Scratch of a stream launch of G CTAs: G partial slots of
 // stream_slot_floats() floats each (O as [D/4][256] float4, then m[256],
-// then l[256]), then G * 8 64-bit flags (one per softmax warp of each CTA).
+// l[256] (exact row sums) and w[256] (row sums of the bf16 weights)), then
+// G * 8 64-bit flags (one per softmax warp of each CTA).
 template <int D>
 __host__ __device__ constexpr int64_t stream_slot_floats() {
-  return static_cast<int64_t>(kTilesPerCta * kBM) * (D + 2);
+  return static_cast<int64_t>(kTilesPerCta * kBM) * (D + 3);
 }
 constexpr int kStreamFlagsPerCta = 8;
 template <int D>
@@ -143,14 +144,15 @@ __device__ __forceinline__ void publish_partial(uint64_t* flag, uint64_t epoch,
 }
 
 // The merger's last step for one row: combine its own accumulator (TMEM at
-// o_addr, reference max m_own, sum l_own) with the partials of CTAs
-// k0 .. k1-1 for the same row (prow within the pair), then store the row
-// (see OutRows) and its LSE as store_final_row does.
+// o_addr, reference max m_own, sums l_own and w_own) with the partials of
+// CTAs k0 .. k1-1 for the same row (prow within the pair), then store the
+// row (see OutRows) and its LSE as store_final_row does: O over the combined
+// bf16-weight sum, the LSE from the combined exact sum.
 template <int D>
 __device__ __forceinline__ void merge_final_row(
-    uint32_t o_addr, float m_own, float l_own, const float* work, int k0,
-    int k1, int prow, __nv_bfloat16* orow, float* lse_at, bool in_range,
-    const OutRows& out) {
+    uint32_t o_addr, float m_own, float l_own, float w_own, const float* work,
+    int k0, int k1, int prow, __nv_bfloat16* orow, float* lse_at,
+    bool in_range, const OutRows& out) {
   const int lane = static_cast<int>(threadIdx.x & 31);
   constexpr int64_t kSlot = stream_slot_floats<D>();
   constexpr int kRows = kTilesPerCta * kBM;
@@ -162,6 +164,7 @@ __device__ __forceinline__ void merge_final_row(
     const float* slot = work + k * kSlot;
     prefetch_l1(slot + D * kRows + prow);
     prefetch_l1(slot + D * kRows + kRows + prow);
+    prefetch_l1(slot + D * kRows + 2 * kRows + prow);
 #pragma unroll
     for (int c4 = 0; c4 < D / 4; ++c4)
       prefetch_l1(reinterpret_cast<const float4*>(slot) + c4 * kRows + prow);
@@ -169,15 +172,18 @@ __device__ __forceinline__ void merge_final_row(
   float M = m_own;
   for (int k = k0; k < k1; ++k)
     M = fmaxf(M, ld_l1(work + k * kSlot + D * kRows + prow));
-  const float w_own = (m_own == -INFINITY) ? 0.f : ex2_approx(m_own - M);
-  float l = l_own * w_own;
+  const float f_own = (m_own == -INFINITY) ? 0.f : ex2_approx(m_own - M);
+  float l = l_own * f_own, wsum = w_own * f_own;
   for (int k = k0; k < k1; ++k) {
     const float* slot = work + k * kSlot;
     const float mk = ld_l1(slot + D * kRows + prow);
-    if (mk != -INFINITY)
-      l += ld_l1(slot + D * kRows + kRows + prow) * ex2_approx(mk - M);
+    if (mk != -INFINITY) {
+      const float fk = ex2_approx(mk - M);
+      l += ld_l1(slot + D * kRows + kRows + prow) * fk;
+      wsum += ld_l1(slot + D * kRows + 2 * kRows + prow) * fk;
+    }
   }
-  const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+  const float inv_l = (wsum > 0.f) ? 1.f / wsum : 0.f;
 #pragma unroll
   for (int cc = 0; cc < D / 32; ++cc) {
     uint32_t orr[32];
@@ -186,7 +192,7 @@ __device__ __forceinline__ void merge_final_row(
     reg_fence32(orr);
     float acc[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(orr[i]) * w_own;
+    for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(orr[i]) * f_own;
     for (int k = k0; k < k1; ++k) {
       const float* slot = work + k * kSlot;
       const float mk = ld_l1(slot + D * kRows + prow);
@@ -480,6 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q_abs = my_row0 + (warp & 3) * 32 + lane;
       float m_ref = -INFINITY;
       float l_run = 0.f;
+      float w_run = 0.f;
       if (publish) {
         // The previous segment's partial is stored: publish it once this
         // segment's first scores exist (Q load and S MMA later), when its
@@ -498,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         softmax_block<D, false>(tmem + lane_off + C::col_s(x),
                                 tmem + lane_off + C::col_p(x), o_addr,
                                 blk * kBN, my_row0, q_abs, p.Nkv, c,
-                                neg_scale, j >= 1, m_ref, l_run);
+                                neg_scale, j >= 1, m_ref, l_run, w_run);
         __syncwarp();
         if (lane == 0) mbar_arrive(bPFull(x));
         blk = (blk + 1 == blk_end) ? blk_lo : blk + 1;
@@ -524,8 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             : 0u,
             &tmO, my_row0 + (warp & 3) * 32, sg.b * p.Hq + sg.hq, p.Nq};
         if (sg.kind == kSegWhole) {
-          store_final_row<D>(o_addr, m_ref, l_run, orow, lse_at, in_range,
-                             out);
+          store_final_row<D>(o_addr, m_ref, l_run, w_run, orow, lse_at,
+                             in_range, out);
         } else if (sg.kind == kSegWriter) {
           float* const slot = p.work + static_cast<int64_t>(blockIdx.x) * kSlot;
           float4* const so = reinterpret_cast<float4*>(slot);
@@ -546,6 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __stcg(slot + D * kRows + prow, m_ref);
           __stcg(slot + D * kRows + kRows + prow, l_run);
+          __stcg(slot + D * kRows + 2 * kRows + prow, w_run);
           // published during the next segment's first block, or below if
           // this is the CTA's last segment
           publish = si + 1 < n_seg;
@@ -561,8 +569,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       kStreamFlagsPerCta,
                           p.epoch, wc));
           if (ok) {
-            merge_final_row<D>(o_addr, m_ref, l_run, p.work, sg.first_cta,
-                               k1, prow, orow, lse_at, in_range, out);
+            merge_final_row<D>(o_addr, m_ref, l_run, w_run, p.work,
+                               sg.first_cta, k1, prow, orow, lse_at, in_range,
+                               out);
             // Consumed: clear the flags so that a replay of this launch
             // waits for its own writers again.
             __syncwarp();

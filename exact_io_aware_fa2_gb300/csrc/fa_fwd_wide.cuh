@@ -75,8 +75,9 @@ struct WideCfg {
       (D == 64 && kSmemUsed < 80 * 1024) ? 80 * 1024 : kSmemUsed;
   static constexpr uint32_t kColO = 2 * kBN;
   // fp32 words of one split-KV partial slot: O rows [128][D] (unnormalised,
-  // relative to the slot's reference max), then m[128], then l[128].
-  static constexpr int64_t kSlotFloats = static_cast<int64_t>(kBM) * (D + 2);
+  // relative to the slot's reference max), then m[128], l[128] (exact row
+  // sums) and w[128] (row sums of the bf16 weights).
+  static constexpr int64_t kSlotFloats = static_cast<int64_t>(kBM) * (D + 3);
   static constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
   // the K ring holds the four softmax warps' staged output rows
   static_assert(4 * 32 * D * 2 <= kKStages * kKVBytes, "output staging");
@@ -293,6 +294,7 @@ __global__ void __launch_bounds__(kWideThreads, WideCfg<D>::kCtasPerSm)
     const int q_abs = row0 + (warp & 3) * 32 + lane;
     float m_ref = -INFINITY;   // reference max (log2 domain) of p and l
     float l_run = 0.f;         // sum of exp2(s*c - m_ref) over seen keys
+    float w_run = 0.f;         // the same sum of the bf16-rounded values
     bool ok = true;
     for (int j = 0; j < nblk; ++j) {
       const int u = j & 1;                      // S buffer of block j
@@ -364,47 +366,16 @@ __global__ void __launch_bounds__(kWideThreads, WideCfg<D>::kCtasPerSm)
           (move && m_ref != -INFINITY) ? ex2_approx(m_ref - m_new) : 1.f;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
 
-      // ---- P = exp2(s * c - m), row sum, pack to bf16 ----
+      // ---- P = exp2(s * c - m), packed to bf16, both row sums ----
       uint32_t pp[BN / 2];
-      float rsum;
-      if (!need_mask) {
-        const uint64_t c2 = f2(c, c);
-        const uint64_t nm2 = f2(-m_use, -m_use);
-        uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int i = 0; i < BN; i += 2) {
-          float x0, x1;
-          f2_split(fma2(f2(S_(i), S_(i + 1)), c2, nm2), x0, x1);
-          const float e0 = ex2_approx(x0);
-          const float e1 = ex2_approx(x1);
-          acc[(i >> 1) & 3] = add2(acc[(i >> 1) & 3], f2(e0, e1));
-          pp[i / 2] = pack_bf16x2(e0, e1);
-        }
-        float s0, s1;
-        f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), s0, s1);
-        rsum = s0 + s1;
-      } else {
-        // the same packed loop; invisible keys get x = -inf, so p = 0
-        const uint64_t c2 = f2(c, c);
-        const uint64_t nm2 = f2(-m_use, -m_use);
-        uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int i = 0; i < BN; i += 2) {
-          float x0, x1;
-          f2_split(fma2(f2(S_(i), S_(i + 1)), c2, nm2), x0, x1);
-          x0 = (i < n_vis) ? x0 : -INFINITY;
-          x1 = (i + 1 < n_vis) ? x1 : -INFINITY;
-          const float e0 = ex2_approx(x0);
-          const float e1 = ex2_approx(x1);
-          acc[(i >> 1) & 3] = add2(acc[(i >> 1) & 3], f2(e0, e1));
-          pp[i / 2] = pack_bf16x2(e0, e1);
-        }
-        float s0, s1;
-        f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), s0, s1);
-        rsum = s0 + s1;
-      }
+      float rsum, wsum;
+      if (!need_mask)
+        exp_pack_row<BN, false>(sr, c, m_use, BN, pp, rsum, wsum);
+      else
+        exp_pack_row<BN, true>(sr, c, m_use, n_vis, pp, rsum, wsum);
 #undef S_
       l_run = l_run * alpha + rsum;
+      w_run = w_run * alpha + wsum;
       m_ref = m_new;
       tmem_st32(tmem + lane_off + static_cast<uint32_t>(u * BN), pp);
 
@@ -467,6 +438,7 @@ __global__ void __launch_bounds__(kWideThreads, WideCfg<D>::kCtasPerSm)
       }
       slot[kBM * D + trow] = nblk > 0 ? m_ref : -INFINITY;
       slot[kBM * D + kBM + trow] = nblk > 0 ? l_run : 0.f;
+      slot[kBM * D + 2 * kBM + trow] = nblk > 0 ? w_run : 0.f;
     } else if (ok && nblk > 0) {
       tc_fence_after();
       const size_t row_idx =
@@ -476,7 +448,7 @@ __global__ void __launch_bounds__(kWideThreads, WideCfg<D>::kCtasPerSm)
       // the four warps' rows for TMA stores.
       const OutRows out{sK + static_cast<uint32_t>(warp & 3) * (32u * D * 2u),
                         &tmO, q_abs - lane, b * p.Hq + hq, p.Nq};
-      store_final_row<D>(o_addr, m_ref, l_run, p.o + row_idx * D,
+      store_final_row<D>(o_addr, m_ref, l_run, w_run, p.o + row_idx * D,
                          p.lse != nullptr ? p.lse + row_idx : nullptr,
                          q_abs < p.Nq, out);
     }

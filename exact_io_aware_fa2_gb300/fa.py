@@ -31,7 +31,7 @@ SYMBOLS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_noalloc",
            "fa_fwd_qk8", "fa_fwd_schedule", "fa_set_schedule", "fa_fwd_host",
            "fa_probe_flag_wait", "fa_fwd_schedule_for",
            "fa_status_string", "fa_last_device_error",
-           "fa_probe_bounded_wait", "fa_version")
+           "fa_probe_bounded_wait", "fa_version", "fa_tensor_map_encodes")
 
 _lib = None
 _lock = threading.Lock()
@@ -97,6 +97,8 @@ def load():
         lib.fa_fwd_schedule_for.argtypes = [ci] * 8 + [pi] * 4 + [
             ctypes.POINTER(ctypes.c_size_t)]
         lib.fa_fwd_schedule_for.restype = ci
+        lib.fa_tensor_map_encodes.argtypes = []
+        lib.fa_tensor_map_encodes.restype = ctypes.c_size_t
         _lib = lib
         return lib
 
@@ -107,6 +109,12 @@ def status_string(status):
 
 def last_device_error():
     return int(load().fa_last_device_error())
+
+
+def tensor_map_encodes():
+    """TMA tensor maps encoded so far (``fa_tensor_map_encodes``); calls on
+    buffers whose maps are cached add nothing."""
+    return int(load().fa_tensor_map_encodes())
 
 
 def probe_bounded_wait(timeout_ns, stream=None):
@@ -248,12 +256,18 @@ def fwd_ws_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, Nq, Nkv, D,
 
 
 def fwd(q, k, v, scale=None, causal=False, out=None, lse=None,
-        want_lse=True, workspace=None):
+        want_lse=True, workspace=None, check=False):
     """Attention forward through the C ABI on the current CUDA stream.
 
     Split-KV scratch (only for shapes that need it) comes from
     ``workspace`` (a uint8 CUDA tensor) or, if None, from torch's caching
-    allocator for this call."""
+    allocator for this call.
+
+    The call returns without synchronising.  A kernel whose bounded wait
+    ran out (``FA_ERR_TIMEOUT``, read by ``last_device_error`` after a
+    synchronisation) leaves the rows it abandoned unwritten; with
+    ``check=True`` the call synchronises the stream, reads that status and
+    raises ``FAError`` if it is set."""
     B, Hq, Hkv, Nq, Nkv, D = _check(q, k, v)
     dev = q.device
     if dev.type != "cuda" or k.device != dev or v.device != dev:
@@ -276,7 +290,19 @@ def fwd(q, k, v, scale=None, causal=False, out=None, lse=None,
                         workspace.data_ptr() if need > 0 else 0, need, stream)
     if st != FA_OK:
         raise FAError(st)
+    if check:
+        _check_device_status(dev, "fa_fwd")
     return out, lse
+
+
+def _check_device_status(dev, what):
+    """Synchronise ``dev``'s current stream and raise if a kernel of the
+    library gave up a bounded wait since the last query."""
+    with torch.cuda.device(dev):
+        torch.cuda.current_stream(dev).synchronize()
+        st = last_device_error()
+    if st != FA_OK:
+        raise FAError(st, what)
 
 
 def fwd_qk8_raw(q8_ptr, k8_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, Nq, Nkv,
@@ -292,9 +318,10 @@ def fwd_qk8_raw(q8_ptr, k8_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, Nq, Nkv,
 
 
 def fwd_qk8(q8, k8, v, scale=None, q_descale=1.0, k_descale=1.0,
-            causal=False, out=None, lse=None):
+            causal=False, out=None, lse=None, check=False):
     """Forward with e4m3 Q and K (``torch.float8_e4m3fn``, with one descale
-    factor each) and bf16 V, through ``fa_fwd_qk8``; D must be 128."""
+    factor each) and bf16 V, through ``fa_fwd_qk8``; D must be 128.
+    ``check`` as for ``fwd``."""
     for name, t, dt in (("q8", q8, torch.float8_e4m3fn),
                         ("k8", k8, torch.float8_e4m3fn),
                         ("v", v, torch.bfloat16)):
@@ -324,7 +351,47 @@ def fwd_qk8(q8, k8, v, scale=None, q_descale=1.0, k_descale=1.0,
                          torch.cuda.current_stream(dev).cuda_stream)
     if st != FA_OK:
         raise FAError(st)
+    if check:
+        _check_device_status(dev, "fa_fwd_qk8")
     return out, lse
+
+
+def _check_host_bufs(bufs, q, k, v):
+    """Every buffer fa_fwd_host reads or writes, against the inputs' shapes:
+    device q, k, v, o bf16 like the inputs and lse fp32 [B, Hq, Nq], all
+    contiguous on one CUDA device; host o_h bf16 and lse_h fp32 of the same
+    shapes, contiguous, on the CPU.  The library copies whole tensors of
+    these sizes, so a smaller buffer would be overrun."""
+    B, Hq, Nq, _ = q.shape
+    want = {"q": (tuple(q.shape), torch.bfloat16, "cuda"),
+            "k": (tuple(k.shape), torch.bfloat16, "cuda"),
+            "v": (tuple(v.shape), torch.bfloat16, "cuda"),
+            "o": (tuple(q.shape), torch.bfloat16, "cuda"),
+            "lse": ((B, Hq, Nq), torch.float32, "cuda"),
+            "o_h": (tuple(q.shape), torch.bfloat16, "cpu"),
+            "lse_h": ((B, Hq, Nq), torch.float32, "cpu")}
+    for name, (shape, dtype, kind) in want.items():
+        t = bufs.get(name)
+        if not isinstance(t, torch.Tensor):
+            raise ValueError(f"bufs[{name!r}] is missing")
+        if tuple(t.shape) != shape:
+            raise ValueError(f"bufs[{name!r}] must have shape {shape}, "
+                             f"not {tuple(t.shape)}")
+        if t.dtype != dtype:
+            raise TypeError(f"bufs[{name!r}] must be {dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"bufs[{name!r}] must be contiguous")
+    dev = None
+    for name, (shape, dtype, kind) in want.items():
+        t = bufs[name]
+        if t.device.type != kind:
+            raise ValueError(f"bufs[{name!r}] must be a {kind} tensor")
+        if kind == "cuda":
+            if dev is None:
+                dev = t.device
+            elif t.device != dev:
+                raise ValueError("the device buffers must share one device")
+    return dev
 
 
 def fwd_host(q, k, v, scale=None, causal=False, device="cuda", bufs=None):
@@ -341,22 +408,24 @@ def fwd_host(q, k, v, scale=None, causal=False, device="cuda", bufs=None):
     _check_host(q, k, v)
     if bufs is None:
         bufs = host_buffers(q, k, v, device)
+    dev = _check_host_bufs(bufs, q, k, v)
     B, Hq, Nq, D = q.shape
     Hkv, Nkv = k.shape[1], k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    dev = bufs["o"].device
-    stream = torch.cuda.current_stream(dev)
-    p = [t.data_ptr() for t in (q, k, v, bufs["o_h"], bufs["lse_h"],
-                                bufs["q"], bufs["k"], bufs["v"], bufs["o"],
-                                bufs["lse"])]
-    st = int(load().fa_fwd_host(*[ctypes.c_void_p(x) for x in p], B, Hq, Hkv,
-                                Nq, Nkv, D, ctypes.c_float(scale),
-                                1 if causal else 0,
-                                ctypes.c_void_p(stream.cuda_stream)))
-    if st != FA_OK:
-        raise FAError(st, "fa_fwd_host")
-    stream.synchronize()
+    # the library works on the current device: make it the buffers' one
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev)
+        p = [t.data_ptr() for t in (q, k, v, bufs["o_h"], bufs["lse_h"],
+                                    bufs["q"], bufs["k"], bufs["v"],
+                                    bufs["o"], bufs["lse"])]
+        st = int(load().fa_fwd_host(*[ctypes.c_void_p(x) for x in p], B, Hq,
+                                    Hkv, Nq, Nkv, D, ctypes.c_float(scale),
+                                    1 if causal else 0,
+                                    ctypes.c_void_p(stream.cuda_stream)))
+        if st != FA_OK:
+            raise FAError(st, "fa_fwd_host")
+        stream.synchronize()
     return bufs["o_h"], bufs["lse_h"]
 
 

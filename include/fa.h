@@ -23,10 +23,29 @@
  * GQA head sharing and the LSE output are this library's specification; the
  * pages do not define them.
  *
- * All functions are thread-safe and callable from any host thread.  Device
- * memory: fa_fwd may take stream-ordered scratch from a per-device pool for
- * the split-KV and stream schedules (see fa_fwd_ws and fa_fwd_schedule);
- * nothing else is allocated.
+ * All functions are thread-safe and callable from any host thread.
+ *
+ * Device memory.  The library's own device memory is the status word read by
+ * fa_last_device_error and the fixed array behind fa_fwd_noalloc, both part
+ * of the loaded module.  One stated exception: fa_fwd, fa_fwd_qk8 and
+ * fa_fwd_host take the scratch some shapes need (split-KV partials, the
+ * stream schedule's partials and flags; fa_fwd_workspace_size gives the
+ * size) from a per-device stream-ordered pool, and that pool keeps up to
+ * 64 MiB of freed scratch reserved between calls so a later call does not
+ * map memory again (on a 152-SM GB300 no shape needs more than about 30 MB;
+ * anything above 64 MiB returns to the device at the next synchronisation).
+ * Callers that want no such reserve use fa_fwd_ws (their own scratch) or
+ * fa_fwd_noalloc (the fixed array).
+ *
+ * Set-up.  The first call into the library on a device (any entry point
+ * that touches the device) checks the compute capability, sets the kernels'
+ * shared-memory limits, creates the pool and looks up the device addresses
+ * of the module's arrays, once per device with that device current; make
+ * that first call before any stream capture on the device.
+ *
+ * TMA tensor maps are encoded on the host and cached per (pointer, extents,
+ * box, element type) in a 64-entry table: repeated calls on the same
+ * buffers encode nothing (fa_tensor_map_encodes counts the encodings).
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -283,9 +302,10 @@ int fa_fwd_host(const void* q_host, const void* k_host, const void* v_host,
  * 152-SM GB300 every supported shape needs at most about 30 MB, so none is
  * rejected there.
  *
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any
- * stream capture.  All calls on a device share the one array: two calls
+ * The array's device address is looked up once per device, with that
+ * device current, by the first call into the library on that device (see
+ * "Set-up" above); make that first call before any stream capture.  All
+ * calls on a device share the one array: two calls
  * whose kernels may overlap on the GPU (different streams, no ordering
  * between them) race on it and can corrupt each other's results.  Calls
  * ordered on one stream are safe.  Each call overwrites every part of the
@@ -331,6 +351,14 @@ int fa_probe_flag_wait(long long timeout_ns, void* stream);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int fa_version(void);
+
+/*
+ * fa_tensor_map_encodes — how many TMA tensor maps the library has encoded
+ * (cuTensorMapEncodeTiled calls) since it was loaded, over all threads and
+ * devices.  A call whose four maps (Q, K, V, O) are in the cache adds
+ * nothing.  For tests and tuning; touches no device.
+ */
+size_t fa_tensor_map_encodes(void);
 
 #ifdef __cplusplus
 }

@@ -154,3 +154,54 @@ def test_host_entry_point_checks_host_pointers_first(lib):
         assert lib.fa_fwd_host(*bad, *dev, *args) == 1
     assert lib.fa_fwd_host(*host[:4], None, *dev, *args) == 1
     assert lib.fa_fwd_host(*host, *dev[:4], None, *args) == 1
+
+
+def test_host_binding_checks_every_buffer_before_any_device_work():
+    """fa.fwd_host checks the caller's buffer set (device q, k, v, o, lse and
+    host o_h, lse_h) against the inputs' shapes, dtypes, layout and device
+    before calling the library, which copies whole tensors of those sizes:
+    a buffer from a smaller shape would be overrun."""
+    import torch
+    q = torch.zeros(2, 4, 8, 64, dtype=torch.bfloat16)
+    k = torch.zeros(2, 2, 16, 64, dtype=torch.bfloat16)
+
+    def bufs(**over):
+        b = {"q": torch.empty(q.shape, dtype=q.dtype, device="meta"),
+             "k": torch.empty(k.shape, dtype=k.dtype, device="meta"),
+             "v": torch.empty(k.shape, dtype=k.dtype, device="meta"),
+             "o": torch.empty(q.shape, dtype=q.dtype, device="meta"),
+             "lse": torch.empty(2, 4, 8, dtype=torch.float32, device="meta"),
+             "o_h": torch.empty(q.shape, dtype=q.dtype),
+             "lse_h": torch.empty(2, 4, 8, dtype=torch.float32)}
+        b.update(over)
+        return {n: t for n, t in b.items() if t is not None}
+
+    small_o = torch.empty(2, 4, 4, 64, dtype=torch.bfloat16)
+    cases = [
+        (ValueError, dict(o=None)),                              # missing
+        (ValueError, dict(o_h=small_o)),                         # smaller
+        (ValueError, dict(lse_h=torch.empty(2, 4, 4))),          # smaller
+        (TypeError, dict(lse_h=torch.empty(2, 4, 8,
+                                           dtype=torch.float64))),
+        (TypeError, dict(o_h=torch.empty(q.shape, dtype=torch.float32))),
+        (ValueError, dict(o_h=torch.empty(2, 4, 64, 8, dtype=torch.bfloat16
+                                          ).transpose(2, 3))),    # strided
+        (ValueError, dict(k=torch.empty(2, 2, 8, 64, dtype=torch.bfloat16,
+                                        device="meta"))),        # wrong N
+    ]
+    for exc, over in cases:
+        with pytest.raises(exc):
+            fa.fwd_host(q, k, k, bufs=bufs(**over))
+    # correct shapes, but the "device" buffers are not CUDA tensors
+    with pytest.raises(ValueError):
+        fa.fwd_host(q, k, k, bufs=bufs())
+    # host outputs on a non-CPU device are refused too
+    with pytest.raises(ValueError):
+        fa.fwd_host(q, k, k, bufs=bufs(
+            o_h=torch.empty(q.shape, dtype=q.dtype, device="meta")))
+
+
+def test_tensor_map_counter_needs_no_device(lib):
+    """fa_tensor_map_encodes reads a host counter: callable without a GPU,
+    and no failed call above encoded anything."""
+    assert fa.tensor_map_encodes() == 0

@@ -66,3 +66,21 @@ def test_maximum_sizes_sampled(B, Hq, Hkv, Nq, Nkv, D, causal):
     # every output row is finite (checked on the device, chunked by batch)
     for b0 in range(0, B, 4096):
         assert torch.isfinite(o[b0:b0 + 4096].float()).all()
+
+
+def test_host_path_with_more_groups_than_four_chunks_of_the_grid_limit():
+    """fa_fwd_host cuts the job into chunks of (batch, kv head) groups and
+    runs each chunk with B = its group count; with 65535 x 8 groups four
+    chunks would pass the grid's 65535 limit, so it uses more.  With one key
+    per head every output row is that key's value row exactly, and the LSE
+    is scale * q . k (closed forms of softmax over one key)."""
+    B, H, D = 65535, 8, 64
+    gen = torch.Generator().manual_seed(5)
+    q = torch.randn(B, H, 1, D, generator=gen).to(torch.bfloat16)
+    k = torch.randn(B, H, 1, D, generator=gen).to(torch.bfloat16)
+    v = torch.randn(B, H, 1, D, generator=gen).to(torch.bfloat16)
+    qp, kp, vp = (t.pin_memory() for t in (q, k, v))
+    o, lse = fa.fwd_host(qp, kp, vp, scale=0.125, causal=False)
+    assert torch.equal(o, v)
+    ref = (q.double() * k.double()).sum(-1) * 0.125
+    assert (lse.double() - ref).abs().max() <= 1e-3

@@ -201,11 +201,15 @@ def test_workload_full_size_sampled(name):
 
 @pytest.mark.parametrize("name", ["pages_b1_h8_q4096_kv8192_d128",
                                   "causal_b4_h16_n2048_d64",
+                                  "causal_gqa_b2_hq32_hkv8_n8192_d128",
+                                  "causal_b1_h16_n32768_d128_large_logits",
                                   "wide_b1_h8_q4096_kv8192_d256",
                                   "stream_b1_h5_q4096_kv8192_d128"])
 def test_workload_full_compare_some_heads(name):
-    """Whole heads of the headline, D=64, D=256 and stream-schedule
-    workloads, element by element."""
+    """Whole heads (the first and the last query head) of the headline,
+    causal D=64, causal GQA, long causal large-logit (32768 x 32768, where
+    the mean |dO| headroom is smallest), D=256 and stream-schedule
+    workloads, element by element against the oracle."""
     w = WORKLOADS[name]
     q, k, v = make_inputs(w)
     o, lse = run_gpu(q, k, v, w.scale, w.causal)
@@ -374,3 +378,45 @@ def test_workspace_missing_or_small_is_rejected():
     assert fa.fwd_ws_raw(*args, ws.data_ptr() + 4, need, s) == 3
     assert fa.fwd_ws_raw(*args, ws.data_ptr(), need, s) == 0
     torch.cuda.synchronize()
+
+
+# ------------------------------------------------------- tensor-map cache
+
+def test_tensor_maps_are_cached_per_pointer_and_shape():
+    """The four TMA maps of a call (Q, K, V, O) are encoded once per
+    (pointer, shape): a repeat call on the same buffers encodes nothing, a
+    new output buffer encodes one map, and results stay identical."""
+    q, k, v = (t.cuda() for t in make_custom(1, 3, 1, 777, 555, 128,
+                                             seed=77))
+    o1 = torch.empty_like(q)
+    lse = torch.empty(1, 3, 777, dtype=torch.float32, device="cuda")
+    n0 = fa.tensor_map_encodes()
+    fa.fwd(q, k, v, out=o1, lse=lse)
+    n1 = fa.tensor_map_encodes()
+    fa.fwd(q, k, v, out=o1, lse=lse)
+    n2 = fa.tensor_map_encodes()
+    o2 = torch.empty_like(q)
+    fa.fwd(q, k, v, out=o2, lse=lse)
+    n3 = fa.tensor_map_encodes()
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+    # a shape used nowhere else: the first call encodes all four maps
+    assert n1 - n0 == 4 and n2 == n1 and n3 - n2 == 1
+    assert torch.equal(o1, o2)
+    O, L = oracle.attention_fp64(q.cpu(), k.cpu(), v.cpu(), 128 ** -0.5,
+                                 False)
+    check(o2.cpu(), lse.cpu(), O, L, "cached maps")
+
+
+def test_check_option_reads_the_device_status():
+    """fwd(check=True) synchronises and raises on a bounded-wait timeout
+    recorded by any kernel of the library; with none recorded it returns
+    normally."""
+    q, k, v = (t.cuda() for t in make_custom(1, 2, 2, 256, 256, 64, seed=78))
+    o, _ = fa.fwd(q, k, v, check=True)
+    assert fa.probe_bounded_wait(2_000_000) == 0    # records FA_ERR_TIMEOUT
+    with pytest.raises(fa.FAError):
+        fa.fwd(q, k, v, check=True)
+    assert fa.last_device_error() == 0              # read and cleared
+    o2, _ = fa.fwd(q, k, v, check=True)
+    assert torch.equal(o, o2)

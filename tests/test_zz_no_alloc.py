@@ -76,6 +76,32 @@ def test_calls_in_a_row_match_fa_fwd():
         print(_compare(shape, seed, causal))
 
 
+def test_calls_leave_device_memory_unchanged():
+    """The property the entry point exists for: a call on a shape that needs
+    scratch takes no device memory.  After one call of each kind (modules
+    loaded, torch's and the pool's memory in place), the free device memory
+    reported by the driver is the same before and after two more no-alloc
+    calls of split shapes."""
+    shape, seed, causal = SPLIT_SHAPES[0]
+    B, Hq, Hkv, Nq, Nkv, D = shape
+    q, k, v = (t.cuda() for t in make_custom(B, Hq, Hkv, Nq, Nkv, D,
+                                             seed=seed))
+    o, lse = _outputs(q)
+    s = torch.cuda.current_stream().cuda_stream
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+            lse.data_ptr(), B, Hq, Hkv, Nq, Nkv, D, D ** -0.5, causal, s)
+    assert fa.fwd_raw(*args) == 0
+    assert fa.fwd_noalloc_raw(*args) == 0
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(2):
+        assert fa.fwd_noalloc_raw(*args) == 0
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert fa.last_device_error() == 0
+    assert free1 == free0, (free0, free1)
+
+
 def test_shape_without_scratch_matches_fa_fwd():
     assert fa.workspace_size(1, 8, 8, 4096, 1024, 128, False) == 0
     print(_compare((1, 8, 8, 4096, 1024, 128), 34, False))
