@@ -193,21 +193,17 @@ __device__ __forceinline__ int kv_blocks(int row0, int Nkv) {
 }
 
 // P = exp2(s * c - m) for the N scores of one row (sr, fp32 bit patterns),
-// packed to bf16x2 into pp (N / 2 words), with two row sums: `exact` of the
-// fp32 values (for the LSE) and `rounded` of the bf16 values, the weights
-// the P V product applies (O is divided by this one, so O / sum is a convex
-// combination of V rows and the rounding of P largely cancels in it).  With
-// MASK, only the first n_vis keys count (the others get p = 0).  The scores
-// are scaled and shifted by one f32x2 FMA per pair, exp2 runs on the MUFU.
+// packed to bf16x2 into pp (N / 2 words); returns the row sum of the fp32
+// values.  With MASK, only the first n_vis keys count (the others get
+// p = 0).  The scores are scaled and shifted by one f32x2 FMA per pair;
+// exp2 runs on the MUFU.
 template <int N, bool MASK>
-__device__ __forceinline__ void exp_pack_row(const uint32_t* sr, float c,
-                                             float m_use, int n_vis,
-                                             uint32_t* pp, float& exact,
-                                             float& rounded) {
+__device__ __forceinline__ float exp_pack_row(const uint32_t* sr, float c,
+                                              float m_use, int n_vis,
+                                              uint32_t* pp) {
   const uint64_t c2 = f2(c, c);
   const uint64_t nm2 = f2(-m_use, -m_use);
-  uint64_t acc[2] = {0, 0};
-  float r[4] = {0.f, 0.f, 0.f, 0.f};
+  uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
   for (int i = 0; i < N; i += 2) {
     float x0, x1;
@@ -220,16 +216,52 @@ __device__ __forceinline__ void exp_pack_row(const uint32_t* sr, float c,
     }
     const float e0 = ex2_approx(x0);
     const float e1 = ex2_approx(x1);
-    const uint32_t pk = pack_bf16x2(e0, e1);
-    pp[i / 2] = pk;
-    acc[(i >> 1) & 1] = add2(acc[(i >> 1) & 1], f2(e0, e1));
-    const int q = ((i >> 1) & 1) * 2;
-    add_bf16x2_to(r[q], r[q + 1], pk);
+    acc[(i >> 1) & 3] = add2(acc[(i >> 1) & 3], f2(e0, e1));
+    pp[i / 2] = pack_bf16x2(e0, e1);
   }
   float s0, s1;
-  f2_split(add2(acc[0], acc[1]), s0, s1);
-  exact = s0 + s1;
-  rounded = (r[0] + r[1]) + (r[2] + r[3]);
+  f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), s0, s1);
+  return s0 + s1;
+}
+
+// Rescale this row's O accumulator (TMEM at o_addr, D fp32 columns) by
+// alpha, for the whole warp when any lane's alpha differs from 1.  S(j)
+// complete means every earlier MMA of the issuing thread, including the P*V
+// of the previous block, is complete, so O is stable here.
+template <int D>
+__device__ __forceinline__ void rescale_o(uint32_t o_addr, float alpha) {
+  if (!__any_sync(0xffffffffu, alpha != 1.f)) return;
+#pragma unroll
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t orr[32];
+    tmem_ld32(o_addr + cc * 32, orr);
+    tmem_ld_wait();
+    reg_fence32(orr);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+    tmem_st32(o_addr + cc * 32, orr);
+  }
+}
+
+// The bf16 rounding error of a block's largest weight: with s_ext the
+// block's extreme score (the one with the largest s * c), the weight is
+// exp2(s_ext * c - m_use), computed as exp_pack_row computes it, and the
+// result is round_bf16(p) - p.  Zero when the block has no visible key.
+//
+// Why: P V applies the bf16-rounded weights, so dividing O by the exact
+// row sum leaves each weight's rounding (up to 2^-8 of it) in O.  When a
+// row's weight concentrates on a few keys (large logits) that is up to
+// 2^-8 |V| on top of O's own bf16 rounding; adding each block's largest
+// weight's rounding to the divisor makes those terms cancel, while the
+// roundings of the many small weights average out.  (On the 32768-key
+// large-logit workload this gives the same largest |dO| as summing every
+// rounded weight, at a few instructions per block instead of two per key.)
+__device__ __forceinline__ float top_rounding(float s_ext, float c,
+                                              float m_use) {
+  const float p = ex2_approx(fmaf(s_ext, c, -m_use));
+  const uint32_t b = pack_bf16x2(p, 0.f);
+  return __uint_as_float(b << 16) - p;
 }
 
 // One K/V block of the online softmax, for the query row this thread owns
@@ -315,34 +347,21 @@ __device__ __forceinline__ void softmax_block(
       (move && m_ref != -INFINITY) ? ex2_approx(m_ref - m_new) : 1.f;
   const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
 
-  // ---- P = exp2(s * c - m), packed to bf16, both row sums ----
+  // the divisor of O also takes the rounding of this block's largest weight
+  w_run = w_run * alpha + (n_vis > 0 ? top_rounding(ext, c, m_use) : 0.f);
+
+  // ---- P = exp2(s * c - m), packed to bf16, row sums ----
   uint32_t pp[kBN / 2];
-  float rsum, wsum;
-  if (!need_mask)
-    exp_pack_row<kBN, false>(sr, c, m_use, kBN, pp, rsum, wsum);
-  else
-    exp_pack_row<kBN, true>(sr, c, m_use, n_vis, pp, rsum, wsum);
+  const float rsum = need_mask
+                         ? exp_pack_row<kBN, true>(sr, c, m_use, n_vis, pp)
+                         : exp_pack_row<kBN, false>(sr, c, m_use, kBN, pp);
 #undef S_
   l_run = l_run * alpha + rsum;
-  w_run = w_run * alpha + wsum;
+  w_run += rsum;
   m_ref = m_new;
 
-  // ---- rescale O when the reference max moved.  S(j) complete means
-  // every earlier MMA of the issuing thread, including the P*V of the
-  // previous block, is complete, so O is stable here. ----
-  if (o_live && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-    for (int cc = 0; cc < D / 32; ++cc) {
-      uint32_t orr[32];
-      tmem_ld32(o_addr + cc * 32, orr);
-      tmem_ld_wait();
-      reg_fence32(orr);
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-      tmem_st32(o_addr + cc * 32, orr);
-    }
-  }
+  // ---- rescale O when the reference max moved ----
+  if (o_live) rescale_o<D>(o_addr, alpha);
   tmem_st32(p_addr, pp);
   tmem_st32(p_addr + 32, pp + 32);
   tmem_st_wait();

@@ -366,16 +366,18 @@ __global__ void __launch_bounds__(kWideThreads, WideCfg<D>::kCtasPerSm)
           (move && m_ref != -INFINITY) ? ex2_approx(m_ref - m_new) : 1.f;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
 
-      // ---- P = exp2(s * c - m), packed to bf16, both row sums ----
+      // the divisor of O also takes the rounding of this block's largest
+      // weight (see top_rounding)
+      w_run = w_run * alpha + (n_vis > 0 ? top_rounding(ext, c, m_use) : 0.f);
+
+      // ---- P = exp2(s * c - m), packed to bf16, row sums ----
       uint32_t pp[BN / 2];
-      float rsum, wsum;
-      if (!need_mask)
-        exp_pack_row<BN, false>(sr, c, m_use, BN, pp, rsum, wsum);
-      else
-        exp_pack_row<BN, true>(sr, c, m_use, n_vis, pp, rsum, wsum);
+      const float rsum =
+          need_mask ? exp_pack_row<BN, true>(sr, c, m_use, n_vis, pp)
+                    : exp_pack_row<BN, false>(sr, c, m_use, BN, pp);
 #undef S_
       l_run = l_run * alpha + rsum;
-      w_run = w_run * alpha + wsum;
+      w_run += rsum;
       m_ref = m_new;
       tmem_st32(tmem + lane_off + static_cast<uint32_t>(u * BN), pp);
 

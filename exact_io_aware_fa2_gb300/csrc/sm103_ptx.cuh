@@ -498,14 +498,4 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// lo += the low bf16 of v, hi += its high bf16 (mixed-precision adds: the
-// bf16 operand is widened exactly, the sum rounded to nearest in fp32).
-__device__ __forceinline__ void add_bf16x2_to(float& lo, float& hi,
-                                              uint32_t v) {
-  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
-      "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
-      : "+f"(lo), "+f"(hi)
-      : "r"(v));
-}
-
 }  // namespace fa
