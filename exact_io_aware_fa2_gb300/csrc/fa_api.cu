@@ -14,6 +14,7 @@
 
 #include "fa.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_fwd_persist.cuh"
 #include "fa_fwd_stream.cuh"
 #include "fa_fwd_wide.cuh"
 
@@ -71,6 +72,13 @@ cudaError_t opt_in_smem_stream() {
                               fa::StreamCfg<D, QK8>::kSmemBytes);
 }
 
+template <int D>
+cudaError_t opt_in_smem_persist() {
+  return cudaFuncSetAttribute(fa::fa_fwd_persist_kernel<D, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              fa::PersistCfg<D, false>::kSmemBytes);
+}
+
 template <int D, bool CAUSAL>
 cudaError_t opt_in_smem_wide() {
   cudaError_t e = cudaFuncSetAttribute(
@@ -87,10 +95,10 @@ cudaError_t opt_in_smem_wide() {
 bool supported_head_dim(int D) {
   return D == 64 || D == 128 || D == 192 || D == 256;
 }
-// Shapes that run the one-tile kernel (fa_fwd_wide.cuh): head dims 192 and
-// 256 always; head dim 64 when causal, where many short CTAs gain from two
-// sharing an SM (measured: causal B4 H16 N2048 503 vs 463 TFLOPS, while the
-// non-causal 4096x8192 shape runs 796 on the two-tile kernel vs 765).
+// Shapes whose split-KV form runs the one-tile kernel (fa_fwd_wide.cuh):
+// head dims 192 and 256 (every schedule), and causal head dim 64 (its
+// one-tile split is finer than the two-tile one; unsplit, causal shapes run
+// the persistent two-tile kernel).
 bool one_tile(int D, int causal) {
   return D == 192 || D == 256 || (D == 64 && causal);
 }
@@ -148,6 +156,8 @@ int device_ready(int** word_out, int* dev_out = nullptr) {
         opt_in_smem_stream<64>() != cudaSuccess ||
         opt_in_smem_stream<128>() != cudaSuccess ||
         opt_in_smem_stream<128, true>() != cudaSuccess ||
+        opt_in_smem_persist<64>() != cudaSuccess ||
+        opt_in_smem_persist<128>() != cudaSuccess ||
         opt_in_smem_wide<64, false>() != cudaSuccess ||
         opt_in_smem_wide<64, true>() != cudaSuccess ||
         opt_in_smem_wide<192, false>() != cudaSuccess ||
@@ -268,19 +278,44 @@ constexpr double kStreamGain = 0.98;
 std::atomic<int> g_forced_schedule{FA_SCHEDULE_AUTO};
 
 struct Plan {
-  int splits;       // split-KV pieces per unit of query rows (1: none)
-  int stream_len;   // K/V blocks per CTA of the stream schedule (0: off)
-  int stream_ctas;  // CTAs of the stream schedule
+  int splits;        // split-KV pieces per unit of query rows (1: none)
+  int stream_len;    // K/V blocks per CTA of the stream schedule (0: off)
+  int stream_ctas;   // CTAs of the stream schedule
+  int persist_ctas;  // CTAs of the persistent schedule (0: off)
 };
 
-Plan plan_forward(int B, int Hq, int Nq, int Nkv, int D, int causal,
-                  int sms) {
+// Persistent schedule (fa_fwd_persist.cuh): causal shapes at head dims 64
+// and 128 that do not split, bf16 inputs, whose K and V together fit in
+// kPersistKVBytes.  One CTA per SM (at most one per pair) walks a list of
+// whole tile pairs sorted longest first over all heads, so at any moment
+// every head's K/V is in use; past L2's reach that re-reads K/V from DRAM
+// (measured on the 16-head 32768-key shape: 2.14 GB read per launch against
+// 0.40 GB with one CTA per pair, which walks the heads in order), and such
+// shapes keep one CTA per pair.  Measured same-GPU against one CTA per pair:
+// causal B4 H16 N2048 D64 63.5 vs 69.2 us, causal GQA B2 Hq32/Hkv8 N8192
+// D128 727 vs 753 us; B1 H16 N32768 D128 2885 vs 2832 us.
+constexpr int64_t kPersistKVBytes = 96ll << 20;
+
+bool persist_ok(int B, int Hkv, int Nkv, int D, int causal, bool qk8) {
+  const int64_t kv_bytes = 4ll * B * Hkv * Nkv * D;     // K and V, bf16
+  return causal && (D == 64 || D == 128) && !qk8 &&
+         kv_bytes <= kPersistKVBytes;
+}
+
+Plan plan_forward(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                  int causal, int sms, bool qk8 = false) {
   const int forced = g_forced_schedule.load(std::memory_order_relaxed);
-  if (forced == FA_SCHEDULE_PLAIN) return Plan{1, 0, 0};
+  if (forced == FA_SCHEDULE_PLAIN) return Plan{1, 0, 0, 0};
   const bool stream_ok = !causal && !one_tile(D, causal);
-  Plan pl{1, 0, 0};
+  Plan pl{1, 0, 0, 0};
   if (forced != FA_SCHEDULE_STREAM || !stream_ok)
     pl.splits = plan_splits(B, Hq, Nq, Nkv, D, causal, sms);
+  if (pl.splits == 1 && persist_ok(B, Hkv, Nkv, D, causal, qk8)) {
+    const int64_t pairs = static_cast<int64_t>(B) * Hq *
+                          ((Nq + 2 * fa::kBM - 1) / (2 * fa::kBM));
+    pl.persist_ctas = static_cast<int>(pairs < sms ? pairs : sms);
+    return pl;
+  }
   if (pl.splits > 1 || !stream_ok) return pl;
   const int64_t pairs = static_cast<int64_t>(B) * Hq *
                         ((Nq + 2 * fa::kBM - 1) / (2 * fa::kBM));
@@ -501,6 +536,16 @@ int launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
   return FA_OK;
 }
 
+template <int D>
+int launch_persist(const CUtensorMap& q, const CUtensorMap& k,
+                   const CUtensorMap& v, const CUtensorMap& o,
+                   const fa::FwdParams& p, int ctas, cudaStream_t stream) {
+  fa::fa_fwd_persist_kernel<D, true>
+      <<<ctas, fa::kThreads, fa::PersistCfg<D, false>::kSmemBytes, stream>>>(
+          q, k, v, o, p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 template <int D, bool CAUSAL>
 int launch_wide(const CUtensorMap& q, const CUtensorMap& k,
                 const CUtensorMap& v, const CUtensorMap& o,
@@ -625,7 +670,8 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
       (qk8 ? static_cast<double>(q_descale) * k_descale : 1.0));
   p.status = word;
   p.wait_limit_ns = kWaitLimitNs;
-  const Plan pl = plan_forward(B, Hq, Nq, Nkv, D, causal, g_sm_count[dev]);
+  const Plan pl =
+      plan_forward(B, Hq, Hkv, Nq, Nkv, D, causal, g_sm_count[dev], qk8);
   p.kv_splits = pl.splits;
   p.work = nullptr;
   p.B = B;
@@ -648,7 +694,8 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
   }
 
   CUtensorMap tq, tk, tv, to;
-  const int kv_rows = one_tile(D, causal) ? fa::WideCfg<256>::kBN : fa::kBN;
+  const bool wide = one_tile(D, causal) && pl.persist_ctas == 0;
+  const int kv_rows = wide ? fa::WideCfg<256>::kBN : fa::kBN;
   const bool qk_ok =
       qk8 ? (encode_bhnd_e4m3(&tq, q, static_cast<long long>(B) * Hq, Nq,
                               D) == FA_OK &&
@@ -666,7 +713,10 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
     if (owned != nullptr) cudaFreeAsync(owned, s);
     return st;
   }
-  if (qk8)
+  if (pl.persist_ctas > 0)
+    st = D == 64 ? launch_persist<64>(tq, tk, tv, to, p, pl.persist_ctas, s)
+                 : launch_persist<128>(tq, tk, tv, to, p, pl.persist_ctas, s);
+  else if (qk8)
     st = causal ? launch<128, true, true>(tq, tk, tv, to, p, B, Hq, Nq, s)
                 : launch<128, false, true>(tq, tk, tv, to, p, B, Hq, Nq, s);
   else if (D == 256)
@@ -675,7 +725,7 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
   else if (D == 192)
     st = causal ? launch_wide<192, true>(tq, tk, tv, to, p, B, Hq, Nq, s)
                 : launch_wide<192, false>(tq, tk, tv, to, p, B, Hq, Nq, s);
-  else if (D == 64 && one_tile(D, causal))
+  else if (D == 64 && wide)
     st = causal ? launch_wide<64, true>(tq, tk, tv, to, p, B, Hq, Nq, s)
                 : launch_wide<64, false>(tq, tk, tv, to, p, B, Hq, Nq, s);
   else if (D == 64)
@@ -733,7 +783,7 @@ int fa_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
   const RunShape rs = run_shape(Hq, Hkv, Nq, causal);
   *bytes = static_cast<size_t>(workspace_bytes(
       B, rs.Hq, rs.Nq, D, causal,
-      plan_forward(B, rs.Hq, rs.Nq, Nkv, D, causal, g_sm_count[dev])));
+      plan_forward(B, rs.Hq, Hkv, rs.Nq, Nkv, D, causal, g_sm_count[dev])));
   return FA_OK;
 }
 
@@ -757,15 +807,17 @@ int fa_fwd_schedule_for(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
     return FA_ERR_INVALID_VALUE;
   if (!supported_head_dim(D)) return FA_ERR_UNSUPPORTED;
   const RunShape rs = run_shape(Hq, Hkv, Nq, causal);
-  const Plan pl = plan_forward(B, rs.Hq, rs.Nq, Nkv, D, causal, sms);
+  const Plan pl = plan_forward(B, rs.Hq, Hkv, rs.Nq, Nkv, D, causal, sms);
   const int64_t rows_u = unit_rows(D, causal);
   const int64_t units = (rs.Nq + rows_u - 1) / rows_u;
-  *kind = pl.stream_len > 0 ? FA_SCHEDULE_STREAM
-          : pl.splits > 1   ? FA_SCHEDULE_SPLIT_KV
-                            : FA_SCHEDULE_PLAIN;
-  *ctas = pl.stream_len > 0
-              ? pl.stream_ctas
-              : static_cast<int>(units * rs.Hq * B * pl.splits);
+  *kind = pl.stream_len > 0     ? FA_SCHEDULE_STREAM
+          : pl.persist_ctas > 0 ? FA_SCHEDULE_PERSIST
+          : pl.splits > 1       ? FA_SCHEDULE_SPLIT_KV
+                                : FA_SCHEDULE_PLAIN;
+  *ctas = pl.stream_len > 0     ? pl.stream_ctas
+          : pl.persist_ctas > 0 ? pl.persist_ctas
+                                : static_cast<int>(units * rs.Hq * B *
+                                                   pl.splits);
   *pieces = pl.splits;
   *blocks_per_cta = pl.stream_len;
   *workspace = static_cast<size_t>(workspace_bytes(B, rs.Hq, rs.Nq, D,

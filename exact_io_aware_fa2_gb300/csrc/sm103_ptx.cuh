@@ -190,6 +190,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Prefetch one box of a tiled tensor into L2 (no shared memory, no
+// completion to wait for); c0 obeys the same alignment rule as a load.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map,
+                                                   int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::
+          "l"(reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 // TMA store of one box from shared memory (bulk-group completion).  Rows
 // outside the tensor are not written.  The generic-proxy writes that filled
 // the box must be made visible to the async proxy first (fence_async_smem).

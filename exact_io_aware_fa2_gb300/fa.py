@@ -179,7 +179,7 @@ def fwd_noalloc_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, Nq, Nkv,
 
 
 # Schedule names of fa_fwd_schedule's FA_SCHEDULE_* values.
-SCHEDULES = {0: "plain", 1: "split_kv", 2: "stream"}
+SCHEDULES = {0: "plain", 1: "split_kv", 2: "stream", 3: "persist"}
 
 
 def schedule(B, Hq, Hkv, Nq, Nkv, D, causal):

@@ -171,7 +171,8 @@ enum {
     FA_SCHEDULE_PLAIN = 0,    /* one CTA per unit of query rows            */
     FA_SCHEDULE_SPLIT_KV = 1, /* key/value ranges split over CTAs, merged
                                  by a second kernel (see fa_fwd_ws)        */
-    FA_SCHEDULE_STREAM = 2    /* equal share of all work per CTA           */
+    FA_SCHEDULE_STREAM = 2,   /* equal share of all work per CTA           */
+    FA_SCHEDULE_PERSIST = 3   /* one CTA per SM over a list of whole units */
 };
 
 /*
@@ -194,6 +195,13 @@ enum {
  *                    kernel).  It relies on CTAs being started in index
  *                    order; a wait that runs out reports FA_ERR_TIMEOUT
  *                    through fa_last_device_error.
+ *                    FA_SCHEDULE_PERSIST (causal mask, D 64 or 128, bf16
+ *                    Q/K, no split, K and V of the call within 96 MiB):
+ *                    at most one CTA per SM, each walking a list of whole
+ *                    pairs of 128-row query tiles, longest first and dealt
+ *                    out in a snake order, so short causal pairs share a
+ *                    CTA's set-up and one pair's epilogue overlaps the next
+ *                    pair's first products.
  *   *ctas            CTAs of the attention kernel
  *   *pieces          key/value ranges per unit (split-KV), else 1
  *   *blocks_per_cta  128-key blocks per CTA (stream), else 0
@@ -223,6 +231,7 @@ int fa_fwd_schedule_for(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
  * an estimate of each schedule's time).
  *
  *   FA_SCHEDULE_PLAIN   one CTA per unit of query rows; also no split-KV
+ *                       and no persistent schedule
  *   FA_SCHEDULE_STREAM  the stream schedule wherever it exists (no causal
  *                       mask, D 64 or 128), with any share per CTA, so a
  *                       pair may be cut into many pieces; other shapes keep

@@ -267,8 +267,9 @@ def test_split_kv_is_used_for_decode_shapes():
     assert kind(1, 8, 8, 128, 32768, 128, False) == "split_kv"
     assert kind(1, 2, 1, 1, 4096, 64, False) == "split_kv"
     assert fa.workspace_size(1, 8, 8, 128, 32768, 128, False) > 0
-    # causal query row 0 sees one key: nothing worth splitting
-    assert kind(1, 2, 1, 1, 4096, 64, True) == "plain"
+    # causal query row 0 sees one key: nothing worth splitting (the causal
+    # shape runs the persistent schedule, which needs no scratch)
+    assert kind(1, 2, 1, 1, 4096, 64, True) == "persist"
     assert fa.workspace_size(1, 2, 1, 1, 4096, 64, True) == 0
     w = WORKLOADS["pages_b1_h8_q4096_kv8192_d128"]
     assert kind(w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D, w.causal) != "split_kv"
@@ -420,3 +421,40 @@ def test_check_option_reads_the_device_status():
     assert fa.last_device_error() == 0              # read and cleared
     o2, _ = fa.fwd(q, k, v, check=True)
     assert torch.equal(o, o2)
+
+
+# ------------------------------------------------------ persistent schedule
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,D", [
+    (4, 16, 16, 2048, 64),      # 512 pairs: 3-4 pairs per CTA
+    (2, 12, 4, 1000, 128),      # ragged tail tile, GQA
+    (1, 3, 1, 300, 64),         # fewer pairs than SMs, tile B ragged
+    (3, 50, 50, 640, 128),      # 450 pairs, pairs without a second tile
+])
+def test_persistent_schedule_matches_one_cta_per_pair(B, Hq, Hkv, N, D):
+    """Causal shapes run persistent CTAs over longest-first lists of tile
+    pairs; the per-pair arithmetic is the two-tile kernel's, so the result
+    equals, bit for bit, the same kernel run one pair per CTA, and matches
+    the oracle on whole heads."""
+    q, k, v = (t.cuda() for t in make_custom(B, Hq, Hkv, N, N, D,
+                                             seed=B * Hq + N))
+    scale = 1.0 / math.sqrt(D)
+    assert fa.schedule(B, Hq, Hkv, N, N, D, True)["kind"] == "persist"
+    o1, l1 = fa.fwd(q, k, v, scale=scale, causal=True)
+    try:
+        fa.set_schedule("plain")
+        o2, l2 = fa.fwd(q, k, v, scale=scale, causal=True)
+    finally:
+        fa.set_schedule("auto")
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+    if D == 128:      # the plain schedule runs the same two-tile kernel
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    g = Hq // Hkv
+    for b, h in {(0, 0), (B - 1, Hq - 1)}:
+        O, L = oracle.attention_fp64(q[b:b + 1, h:h + 1].cpu(),
+                                     k[b:b + 1, h // g:h // g + 1].cpu(),
+                                     v[b:b + 1, h // g:h // g + 1].cpu(),
+                                     scale, True)
+        print(check(o1[b:b + 1, h:h + 1].cpu(), l1[b:b + 1, h:h + 1].cpu(),
+                    O, L, f"persist B{B} H{Hq}/{Hkv} N{N} D{D} b{b} h{h}"))

@@ -69,6 +69,31 @@ def test_causal_and_wide_shapes_never_stream():
         fa.set_schedule("auto")
 
 
+@pytest.mark.parametrize("shape,ctas", [
+    ((4, 16, 16, 2048, 2048, 64, True), 152),      # 512 pairs, 32 MiB K/V
+    ((2, 32, 8, 8192, 8192, 128, True), 152),      # 2048 pairs, 64 MiB K/V
+    ((1, 2, 2, 512, 512, 128, True), 4),           # fewer pairs than SMs
+])
+def test_causal_shapes_run_persistent(shape, ctas):
+    """Causal shapes at head dims 64 and 128 that do not split, and whose K
+    and V fit in 96 MiB, run the persistent schedule: at most one CTA per
+    SM, no scratch; forcing the plain schedule turns it off."""
+    s = sched(*shape)
+    assert s == {"kind": "persist", "ctas": ctas, "pieces": 1,
+                 "blocks_per_cta": 0, "workspace": 0}
+    fa.set_schedule("plain")
+    assert sched(*shape)["kind"] == "plain"
+
+
+def test_causal_shapes_with_large_kv_run_one_pair_per_cta():
+    """Past 96 MiB of K and V (here 256 MiB: 16 heads of 32768 keys) the
+    longest-first list would keep every head's K/V in use at once and
+    re-read it from DRAM; such shapes run one CTA per pair, whose grid
+    walks the heads in order."""
+    s = sched(1, 16, 16, 32768, 32768, 128, True)
+    assert s["kind"] == "plain" and s["ctas"] == 16 * 128
+
+
 def test_forced_settings():
     fa.set_schedule("plain")
     s = sched(1, 8, 8, 128, 32768, 128)
@@ -110,6 +135,15 @@ def test_invariants(sms):
             if s["kind"] == "plain":
                 assert s["ctas"] == units and s["pieces"] == 1, what
                 assert s["workspace"] == 0, what
+            elif s["kind"] == "persist":
+                pairs = math.ceil(N / 256) * H * B
+                assert causal and D in (64, 128), what
+                assert s["ctas"] == min(pairs, sms), what
+                assert s["pieces"] == 1 and s["workspace"] == 0, what
+                assert 4 * B * Hkv * Nkv * D <= 96 << 20, what
+                assert pairs * 2 > sms or sched(B, Hq, Hkv, Nq, Nkv, D,
+                                                causal, sms)["kind"] == \
+                    "persist", what
             elif s["kind"] == "split_kv":
                 keys = 64 if one_tile else 128
                 longest = math.ceil((min(N, Nkv) if causal else Nkv) / keys)
