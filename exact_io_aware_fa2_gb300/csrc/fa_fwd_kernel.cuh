@@ -83,9 +83,10 @@ struct FwdCfg {
   // loads are then issued two iterations ahead of their use.
   static constexpr int kKStages = (D == 128) ? (QK8 ? 4 : 2) : 4;
   static constexpr int kVStages = (D == 128) ? 3 : 4;
-  // barriers: Q, K full/empty, V full/empty, S full x2, P full x2, O final,
-  // drain
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1 + 1;
+  // barriers: Q of tile A, K full/empty, V full/empty, S full x2, P full
+  // x2, O final, drain, Q of tile B
+  static constexpr int kNumBars =
+      1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1 + 1 + 1;
   // + tmem slot (8 bytes with padding) + the wait state (24 bytes)
   static constexpr int kBarBytes = 8 * kNumBars + 32;
   static constexpr int kSmemBytes =
@@ -517,6 +518,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bPFull = [&](int x) { return bar(kB0 + 2 + x); };
   const uint32_t bOFinal = bar(kB0 + 4);
   const uint32_t bDrain = bar(kB0 + 5);
+  // Q of tile A at bQFull, of tile B here: S_A(first) waits only for Q_A
+  const uint32_t bQFullB = bar(kB0 + 6);
   uint8_t* const misc = base_ptr + (sBar - base) + 8 * C::kNumBars;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   WaitState* const wstate = reinterpret_cast<WaitState*>(misc + 8);
@@ -537,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bOFinal, 1);
     mbar_init(bDrain, 1);
+    mbar_init(bQFullB, 1);
     wstate->abort = 0u;
     wstate->status = p.status;
     wstate->limit_ns = p.wait_limit_ns;
@@ -562,11 +566,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t once = l2_policy_evict_first();
       const int zq = b * p.Hq + hq;
       const int zk = b * p.Hkv + hk;
-      mbar_arrive_expect_tx(bQFull, C::kQKTileBytes * (has_b ? 2 : 1));
-      for (int x = 0; x < (has_b ? 2 : 1); ++x)
+      // Order of the first loads: Q_A, K_0, then Q_B, so S_A(0) can start
+      // once the first two have landed (at the start every CTA loads from
+      // DRAM at once).
+      auto load_q = [&](int x, uint32_t qbar) {
+        mbar_arrive_expect_tx(qbar, C::kQKTileBytes);
         for (int c = 0; c < C::kQKBoxes; ++c)
-          tma_load_3d(sQ + x * C::kQKTileBytes + c * kBoxBytes, &tmQ, bQFull,
+          tma_load_3d(sQ + x * C::kQKTileBytes + c * kBoxBytes, &tmQ, qbar,
                       c * C::kQKBoxCols, row0[x], zq, once);
+      };
+      load_q(0, bQFull);
+      bool q_b_issued = false;
       int k_issued = 0, v_issued = 0;
       for (int i = 0; i < n_blocks; ++i) {
         const int j = j0 + i;                    // block index in the pair
@@ -577,6 +587,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sK + sk * C::kQKTileBytes + c * kBoxBytes, &tmK,
                       bKFull(sk), c * C::kQKBoxCols, j * kBN, zk, keep);
         k_issued = i + 1;
+        if (has_b && !q_b_issued) {
+          load_q(1, bQFullB);
+          q_b_issued = true;
+        }
         if (!mbar_wait(bVEmpty(sv), ((i / NV) & 1) ^ 1, wc)) break;
         mbar_arrive_expect_tx(bVFull(sv), C::kTileBytes);
         for (int c = 0; c < C::kBoxes; ++c)
@@ -591,6 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = (v_issued > NV ? v_issued - NV : 0); j < v_issued; ++j)
         mbar_wait(bVFull(j % NV), (j / NV) & 1, wc, false);
       mbar_wait(bQFull, 0, wc, false);
+      if (q_b_issued) mbar_wait(bQFullB, 0, wc, false);
     }
   } else if (warp == kMmaWarp) {
     // ============================ MMA issuer ==============================
@@ -631,6 +646,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // S_x(j) = Q_x K_j^T
         if (j < n_blocks && j0 + j < nblk[x]) {
+          if (x == 1 && j == 0 &&
+              !(ok = __all_sync(kAll, mbar_wait(bQFullB, 0, wc))))
+            break;
           issue_qk<D, QK8>(tmem + C::col_s(x),
                            dQ + static_cast<uint64_t>(x) * kQKStep, dKs,
                            C::kIdescS);

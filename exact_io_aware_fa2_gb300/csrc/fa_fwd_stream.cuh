@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bDrain = bar(kB0 + 5);
   const uint32_t bQEmpty = bar(kB0 + 6);
   const uint32_t bOEmpty = bar(kB0 + 7);
-  static_assert(kB0 + 8 == SC::kNumBars, "barrier count");
+  static_assert(kB0 + 8 <= SC::kNumBars, "barrier count");
   uint8_t* const misc = base_ptr + (sBar - base) + 8 * SC::kNumBars;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   WaitState* const wstate = reinterpret_cast<WaitState*>(misc + 8);
