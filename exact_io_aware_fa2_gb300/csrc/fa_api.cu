@@ -517,6 +517,11 @@ int launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             ((p.Nkv + fa::kBN - 1) / fa::kBN);
       const dim3 sgrid(static_cast<unsigned>(
           (total + p.stream_len - 1) / p.stream_len));
+      // the CTAs' ticket counter starts at zero on every launch
+      if (cudaMemsetAsync(reinterpret_cast<char*>(p.work) +
+                              fa::stream_ticket_offset<D>(sgrid.x),
+                          0, 8, stream) != cudaSuccess)
+        return FA_ERR_CUDA;
       fa::fa_fwd_stream_kernel<D, QK8>
           <<<sgrid, fa::kThreads, fa::StreamCfg<D, QK8>::kSmemBytes,
              stream>>>(q, k, v, o, p);

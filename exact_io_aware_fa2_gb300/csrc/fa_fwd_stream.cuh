@@ -27,9 +27,12 @@
 // Ordering: a CTA runs its segments from its last pair down to its first,
 // so its writer segment (if any) comes first and its merger segment (if
 // any) last, and a merger depends only on CTAs with lower indices, whose
-// writer segments ran at their start.  This relies on CTAs being started in
-// index order (the grid has at most one CTA per SM); every wait is bounded
-// and reports FA_ERR_TIMEOUT if it runs out.  A writer publishes its
+// writer segments ran at their start.  The index is not the CTA's grid
+// index but a ticket each CTA draws from a counter in the scratch (zeroed
+// before the launch) when it starts: a lower index then always belongs to a
+// CTA that is already running, whatever order the hardware starts CTAs in
+// and whatever else shares the GPU.  Every wait is bounded and reports
+// FA_ERR_TIMEOUT if it runs out.  A writer publishes its
 // partial per softmax warp with a fence and a release store of the launch's
 // epoch to a flag, once the next segment's first scores exist (its stores
 // have drained by then); the merger's warp waits (bounded, acquire) for that
@@ -67,10 +70,11 @@ struct StreamRange {
 };
 
 __device__ __forceinline__ StreamRange stream_range(const FwdParams& p,
-                                                    int n_pairs, int nbp) {
+                                                    int n_pairs, int nbp,
+                                                    int cta) {
   const int64_t total = static_cast<int64_t>(p.B) * p.Hq * n_pairs * nbp;
   StreamRange r;
-  r.start = static_cast<int64_t>(blockIdx.x) * p.stream_len;
+  r.start = static_cast<int64_t>(cta) * p.stream_len;
   r.end = min(r.start + p.stream_len, total);
   r.n_seg = r.start < r.end
                 ? static_cast<int>((r.end - 1) / nbp - r.start / nbp + 1)
@@ -116,16 +120,20 @@ __device__ __forceinline__ StreamSeg stream_segment(const FwdParams& p,
 // Scratch of a stream launch of G CTAs: G partial slots of
 // stream_slot_floats() floats each (O as [D/4][256] float4, then m[256],
 // l[256] (exact row sums) and w[256] (row sums of the bf16 weights)), then
-// G * 8 64-bit flags (one per softmax warp of each CTA).
+// G * 8 64-bit flags (one per softmax warp of each CTA), then the 64-bit
+// ticket counter (zeroed before each launch) and 8 bytes of padding.
 template <int D>
 __host__ __device__ constexpr int64_t stream_slot_floats() {
   return static_cast<int64_t>(kTilesPerCta * kBM) * (D + 3);
 }
 constexpr int kStreamFlagsPerCta = 8;
 template <int D>
+__host__ __device__ constexpr int64_t stream_ticket_offset(int64_t ctas) {
+  return ctas * stream_slot_floats<D>() * 4 + ctas * kStreamFlagsPerCta * 8;
+}
+template <int D>
 __host__ __device__ constexpr int64_t stream_workspace_bytes(int64_t ctas) {
-  return ctas * stream_slot_floats<D>() * 4 +
-         ctas * kStreamFlagsPerCta * 8;
+  return stream_ticket_offset<D>(ctas) + 16;
 }
 
 __device__ __forceinline__ void prefetch_l1(const void* ptr) {
@@ -246,8 +254,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int n_pairs = (p.Nq + 2 * kBM - 1) / (2 * kBM);
   const int nbp = (p.Nkv + kBN - 1) / kBN;          // K/V blocks per pair
-  const StreamRange range = stream_range(p, n_pairs, nbp);
-  const int n_seg = range.n_seg;
+
+  // This CTA's index: a ticket drawn when it starts (see the header).  The
+  // index and the CTA's range of items sit in shared memory and are read
+  // where used, which keeps them out of the registers of the block loops.
+  __shared__ StreamRange range_s;
+  __shared__ int cta_s;
+  if (threadIdx.x == 0) {
+    const int t = static_cast<int>(atomicAdd(
+        reinterpret_cast<unsigned long long*>(
+            reinterpret_cast<char*>(p.work) +
+            stream_ticket_offset<D>(gridDim.x)),
+        1ull));
+    cta_s = t;
+    range_s = stream_range(p, n_pairs, nbp, t);
+  }
+  __syncthreads();
+  auto cta_index = [&]() -> int { return *static_cast<volatile int*>(&cta_s); };
+  auto range = [&]() {
+    const volatile StreamRange& r = range_s;
+    return StreamRange{r.start, r.end, r.n_seg};
+  };
+  auto n_seg = [&]() -> int {
+    return *static_cast<volatile int*>(&range_s.n_seg);
+  };
 
   // ---- shared memory carve-up (as the two-tile kernel, two more barriers)
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -320,8 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int r = 0, k_issued = 0, v_issued = 0, q_loads = 0;
       int sk = 0, kph = 0, sv = 0, vph = 0;
       bool ok = true;
-      for (int si = 0; ok && si < n_seg; ++si) {
-        const StreamSeg sg = stream_segment(p, range, n_pairs, nbp, si);
+      for (int si = 0; ok && si < n_seg(); ++si) {
+        const StreamSeg sg = stream_segment(p, range(), n_pairs, nbp, si);
         const int row0 = sg.pair * (2 * kBM);
         const bool has_b = row0 + kBM < p.Nq;
         const int zq = sg.b * p.Hq + sg.hq;
@@ -382,11 +412,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ks = 0, kph = 0;      // stage and phase of the next K block
     int vs = 0, vph = 0;      // stage and phase of the next V block
     uint32_t pph = 0;         // bit x: phase of tile x's next P
-    for (int si = 0; ok && si < n_seg; ++si) {
+    for (int si = 0; ok && si < n_seg(); ++si) {
       bool live_b;
       int n_blocks;
       {
-        const StreamSeg sg = stream_segment(p, range, n_pairs, nbp, si);
+        const StreamSeg sg = stream_segment(p, range(), n_pairs, nbp, si);
         live_b = sg.pair * (2 * kBM) + kBM < p.Nq;
         n_blocks = sg.n;
       }
@@ -466,17 +496,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto my_flag = [&]() {
       return reinterpret_cast<uint64_t*>(
                  p.work + static_cast<int64_t>(gridDim.x) * kSlot) +
-             static_cast<int64_t>(blockIdx.x) * kStreamFlagsPerCta + role;
+             static_cast<int64_t>(cta_index()) * kStreamFlagsPerCta + role;
     };
     uint32_t sph = 0;          // phase of this tile's next S
     bool ok = true;
     bool publish = false;      // this warp's partial is stored, unpublished
-    for (int si = 0; si < n_seg; ++si) {
+    for (int si = 0; si < n_seg(); ++si) {
       // Only what the block loop needs stays live across it; the epilogue
       // recomputes the rest of the segment's description.
       int my_row0, nb, blk, blk_lo, blk_end;
       {
-        const StreamSeg sg = stream_segment(p, range, n_pairs, nbp, si);
+        const StreamSeg sg = stream_segment(p, range(), n_pairs, nbp, si);
         my_row0 = sg.pair * (2 * kBM) + x * kBM;
         nb = (x == 0 || my_row0 < p.Nq) ? sg.n : 0;
         blk = sg.first;                          // block index in the pair
@@ -516,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bOFinal, si & 1, wc));
       if (ok && nb > 0) {
         tc_fence_after();
-        const StreamSeg sg = stream_segment(p, range, n_pairs, nbp, si);
+        const StreamSeg sg = stream_segment(p, range(), n_pairs, nbp, si);
         const size_t row_idx =
             (static_cast<size_t>(sg.b) * p.Hq + sg.hq) *
                 static_cast<size_t>(p.Nq) +
@@ -527,14 +557,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // In the CTA's last segment every MMA is complete and every K tile
         // consumed: the K ring stages the output rows for TMA stores.
         const OutRows out{
-            si + 1 == n_seg ? sK + static_cast<uint32_t>(role) * (32u * D * 2u)
+            si + 1 == n_seg() ? sK + static_cast<uint32_t>(role) * (32u * D * 2u)
                             : 0u,
             &tmO, my_row0 + (warp & 3) * 32, sg.b * p.Hq + sg.hq, p.Nq};
         if (sg.kind == kSegWhole) {
           store_final_row<D>(o_addr, m_ref, l_run, w_run, orow, lse_at,
                              in_range, out);
         } else if (sg.kind == kSegWriter) {
-          float* const slot = p.work + static_cast<int64_t>(blockIdx.x) * kSlot;
+          float* const slot =
+              p.work + static_cast<int64_t>(cta_index()) * kSlot;
           float4* const so = reinterpret_cast<float4*>(slot);
           constexpr int kRows = kTilesPerCta * kBM;
 #pragma unroll
@@ -556,10 +587,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           __stcg(slot + D * kRows + 2 * kRows + prow, w_run);
           // published during the next segment's first block, or below if
           // this is the CTA's last segment
-          publish = si + 1 < n_seg;
+          publish = si + 1 < n_seg();
           if (!publish) publish_partial(my_flag(), p.epoch, lane);
         } else {
-          const int k1 = static_cast<int>(blockIdx.x);
+          const int k1 = cta_index();
           uint64_t* const flags = my_flag() - static_cast<int64_t>(k1) *
                                                   kStreamFlagsPerCta;
           for (int k = sg.first_cta; ok && k < k1; ++k)

@@ -102,7 +102,7 @@ def test_forced_settings():
     # one block per CTA when there are fewer blocks than SMs: 2 pairs of 24
     s = sched(1, 2, 2, 256, 3000, 128)
     assert s["kind"] == "stream" and s["blocks_per_cta"] == 1
-    assert s["ctas"] == 48 and s["workspace"] == 48 * (SLOT[128] + 64)
+    assert s["ctas"] == 48 and s["workspace"] == 48 * (SLOT[128] + 64) + 16
     fa.set_schedule("auto")
     assert sched(1, 2, 2, 256, 3000, 128)["kind"] != "stream"
 
@@ -161,4 +161,4 @@ def test_invariants(sms):
                 assert L == math.ceil(total / sms), what
                 assert s["ctas"] == math.ceil(total / L) <= sms, what
                 assert 2 * L >= nbp, what
-                assert s["workspace"] == s["ctas"] * (SLOT[D] + 64), what
+                assert s["workspace"] == s["ctas"] * (SLOT[D] + 64) + 16, what
