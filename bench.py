@@ -27,7 +27,10 @@ and in the same way, for comparison (``--no-sdpa`` skips it).  Its
 ``configs`` object times each of the five workloads the metric is specified
 on (tiny, the pages' shape, causal D64, causal GQA, long causal with large
 logits) in this process with the same steps, warm-up and L2 flush
-(``--no-configs`` skips it); ``value`` stays the chosen workload's.
+(``--no-configs`` skips it); ``value`` stays the chosen workload's.  With
+the configs, a head-dim-128 workload also gets ``low_precision``: the same
+shape with Q and K in e4m3 (per-tensor descales) and in MXFP8 (a ue8m0
+scale per 32 elements), timed the same way.
 """
 
 import argparse
@@ -45,7 +48,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from exact_io_aware_fa2_gb300.workloads import (HEADLINE, WORKLOADS,  # noqa
-                                                make_inputs, quantize_e4m3)
+                                                make_inputs, quantize_e4m3,
+                                                quantize_mxfp8)
 
 METRIC = ("attention fwd TFLOPS (4·B·H·Nq·Nkv·D, "
           "causal ½) and % of GB300 BF16 peak")
@@ -129,24 +133,33 @@ def peaks():
 # file leave recorded counters valid).
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ("fa_fwd_kernel.cuh", "sm103_ptx.cuh"),
+    "fa_fwd_persist_kernel": ("fa_fwd_persist.cuh", "fa_fwd_kernel.cuh",
+                              "sm103_ptx.cuh"),
     "fa_fwd_stream_kernel": ("fa_fwd_stream.cuh", "fa_fwd_kernel.cuh",
                              "sm103_ptx.cuh"),
     "fa_fwd_wide_kernel": ("fa_fwd_wide.cuh", "fa_fwd_kernel.cuh",
                            "sm103_ptx.cuh"),
+    "fa_fwd_mx_kernel": ("fa_fwd_mx.cuh", "fa_fwd_wide.cuh",
+                         "fa_fwd_kernel.cuh", "sm103_ptx.cuh"),
 }
 
 
 def kernel_for(w):
-    """The attention kernel that runs a workload on this device (head dims
-    192 and 256, and causal shapes at head dim 64, take the one-tile kernel;
-    the stream schedule has its own kernel)."""
-    one_tile = w.D in (192, 256) or (w.D == 64 and w.causal)
-    if one_tile:
-        return "fa_fwd_wide_kernel"
+    """The attention kernel that runs a workload on this device: head dims
+    192 and 256 (and split causal shapes at 64) take the one-tile kernel,
+    the stream and persistent schedules and MXFP8 inputs have kernels of
+    their own, the rest run the two-tile kernel."""
     from exact_io_aware_fa2_gb300 import fa
+    if w.mx:
+        return "fa_fwd_mx_kernel"
     sch = fa.schedule(w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D, w.causal)
-    return "fa_fwd_stream_kernel" if sch["kind"] == "stream" \
-        else "fa_fwd_kernel"
+    if sch["kind"] == "stream":
+        return "fa_fwd_stream_kernel"
+    if sch["kind"] == "persist":
+        return "fa_fwd_persist_kernel"
+    if w.D in (192, 256) or (w.D == 64 and w.causal):
+        return "fa_fwd_wide_kernel"
+    return "fa_fwd_kernel"
 
 
 def kernel_source_hash(kernel="fa_fwd_kernel"):
@@ -377,7 +390,7 @@ def sdpa_column(w, q, k, v, o_ours, flush, stream, steps, warmup=5):
         except Exception as exc:  # a backend this GPU/torch cannot run
             entry = {"unavailable": f"{type(exc).__name__}: "
                                     f"{str(exc).splitlines()[0][:160]}"}
-        if w.qk8 and "unavailable" not in entry:
+        if (w.qk8 or w.mx) and "unavailable" not in entry:
             entry["note"] = (entry.get("note", "") +
                              " bf16 Q/K/V: torch SDPA takes no e4m3 inputs"
                              ).strip()
@@ -456,6 +469,56 @@ def spec_configs(args, fa, flush, stream, dev, headline):
     return out
 
 
+def low_precision_column(args, fa, w, q_h, k_h, v, o_bf16, lse_bf16, flush,
+                         stream, dev):
+    """The same workload with Q and K in 8 bits, timed like the headline:
+    e4m3 with one descale per tensor (fa_fwd_qk8) and MXFP8, e4m3 with a
+    ue8m0 scale per 32 elements (fa_fwd_mxfp8).  TFLOPS from the mean step,
+    the fraction of the peak for half the flops at the e4m3 rate (4/3 of the
+    bf16 peak) and of the bf16 peak, and the largest difference from the
+    bf16 path's O and LSE on these inputs (the inputs' quantisation, not a
+    parity measure: parity of both paths is against the oracle on the
+    dequantised inputs)."""
+    peak, _ = peaks()
+    o = torch.empty_like(o_bf16)
+    lse = torch.empty_like(lse_bf16)
+    (q8e, qd), (k8e, kd) = quantize_e4m3(q_h), quantize_e4m3(k_h)
+    q8e, k8e = q8e.to(dev), k8e.to(dev)
+    (q8m, qs), (k8m, ks) = quantize_mxfp8(q_h), quantize_mxfp8(k_h)
+    q8m, k8m, qs, ks = (t.to(dev) for t in (q8m, k8m, qs, ks))
+    runs = {
+        "qk8": ("fa_fwd_kernel (QK8)", lambda: fa.fwd_qk8(
+            q8e, k8e, v, scale=w.scale, q_descale=qd, k_descale=kd,
+            causal=w.causal, out=o, lse=lse)),
+        "mxfp8": ("fa_fwd_mx_kernel", lambda: fa.fwd_mxfp8(
+            q8m, k8m, v, qs, ks, scale=w.scale, causal=w.causal, out=o,
+            lse=lse)),
+    }
+    out = {}
+    for name, (kernel, launch) in runs.items():
+        def sync():
+            torch.cuda.synchronize(dev)
+        starts, ends = time_steps(launch, flush, stream, args.steps,
+                                  args.warmup, sync)
+        sync()
+        if fa.last_device_error() != 0:
+            raise RuntimeError(f"bounded-wait timeout timing {name}")
+        per = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        mean = sum(per) / len(per)
+        tf = w.flops / (mean * 1e-3) / 1e12
+        out[name] = {
+            "workload": w.name, "value": tf, "unit": UNIT,
+            "ms_per_step": mean, "ms_per_step_median": statistics.median(per),
+            "frac_of_e4m3_qk_peak": tf / (peak * 4.0 / 3.0),
+            "frac_of_bf16_peak": tf / peak, "steps": args.steps,
+            "kernel": kernel,
+            "max_abs_diff_o_vs_bf16_path":
+                float((o.float() - o_bf16.float()).abs().max()),
+            "max_abs_diff_lse_vs_bf16_path":
+                float((lse - lse_bf16).abs().max())}
+    return out
+
+
 def run_ours(args, w):
     from exact_io_aware_fa2_gb300 import fa
     ws, rank, local = dist_env()
@@ -481,11 +544,18 @@ def run_ours(args, w):
         # e4m3 Q and K with per-tensor descales (the fa_fwd_qk8 path)
         (q8_h, qd), (k8_h, kd) = quantize_e4m3(q_h), quantize_e4m3(k_h)
         q8, k8 = q8_h.to(dev), k8_h.to(dev)
+    if w.mx:
+        # MXFP8 Q and K: e4m3 with a ue8m0 scale per 32 elements
+        (q8_h, qs_h), (k8_h, ks_h) = quantize_mxfp8(q_h), quantize_mxfp8(k_h)
+        q8, k8, qs, ks = (t.to(dev) for t in (q8_h, k8_h, qs_h, ks_h))
 
     def launch():
         if w.qk8:
             fa.fwd_qk8(q8, k8, v, scale=w.scale, q_descale=qd, k_descale=kd,
                        causal=w.causal, out=o, lse=lse)
+        elif w.mx:
+            fa.fwd_mxfp8(q8, k8, v, qs, ks, scale=w.scale, causal=w.causal,
+                         out=o, lse=lse)
         else:
             fa.fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse)
 
@@ -510,8 +580,13 @@ def run_ours(args, w):
             raise RuntimeError("bounded-wait timeout during the timed loop")
         per = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
         configs = None
+        lowp = None
         if ws == 1 and not args.no_configs:
             configs = spec_configs(args, fa, flush, stream, dev, w)
+            if not (w.qk8 or w.mx) and w.D == 128:
+                launch()
+                lowp = low_precision_column(args, fa, w, q_h, k_h, v, o,
+                                            lse, flush, stream, dev)
     ms = sum(per) / len(per)
     ms_max = max_over_ranks(ms, dev)
     value = job_tflops(w.flops, ms_max, ws)
@@ -522,7 +597,7 @@ def run_ours(args, w):
     hbm_gbs = traffic / (ms * 1e-3) / 1e9 if traffic else None
     hbm_frac = (hbm_gbs / hbm_peak()) if hbm_gbs and hbm_peak() else None
     peak_src += ", of measured" if "MEASURED" in peak_src else ", of fallback"
-    if w.qk8:
+    if w.qk8 or w.mx:
         # Half the flops (Q K^T) run as e4m3 products at twice the bf16 rate
         # (the nominal 4.5 vs 2.25 PFLOP/s), half (P V) at the bf16 rate:
         # the step's peak is 2 / (1/(2P) + 1/P) = 4P/3.
@@ -535,8 +610,8 @@ def run_ours(args, w):
     launches_per_step = 2 if split else 1
 
     # ---- end to end through the public API with host buffers ----
-    if w.qk8:
-        host_in = (q8_h, k8_h, v_h)
+    if w.qk8 or w.mx:
+        host_in = (q8_h, k8_h, v_h) + ((qs_h, ks_h) if w.mx else ())
         pinned = [t.pin_memory() for t in host_in]
         dev_in = [torch.empty_like(t, device=dev) for t in host_in]
         o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
@@ -545,9 +620,13 @@ def run_ours(args, w):
         def e2e_step():
             for d_, h_ in zip(dev_in, pinned):
                 d_.copy_(h_, non_blocking=True)
-            fa.fwd_qk8(dev_in[0], dev_in[1], dev_in[2], scale=w.scale,
-                       q_descale=qd, k_descale=kd, causal=w.causal, out=o,
-                       lse=lse)
+            if w.mx:
+                fa.fwd_mxfp8(*dev_in, scale=w.scale, causal=w.causal, out=o,
+                             lse=lse)
+            else:
+                fa.fwd_qk8(dev_in[0], dev_in[1], dev_in[2], scale=w.scale,
+                           q_descale=qd, k_descale=kd, causal=w.causal,
+                           out=o, lse=lse)
             o_h.copy_(o, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)
             torch.cuda.current_stream(dev).synchronize()
@@ -589,7 +668,8 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 QK^T, bf16 PV" if w.qk8 else "bf16",
+        "dtype": "e4m3 QK^T, bf16 PV" if w.qk8 else
+                 "mxfp8 QK^T (e4m3, ue8m0 per 32), bf16 PV" if w.mx else "bf16",
         "data": "synthetic",
         "pct_of_peak": 100.0 * per_launch_tflops / peak,
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
@@ -622,6 +702,7 @@ def run_ours(args, w):
             statistics.median(per),
         "ms_per_step_all": per,
         "configs": configs,
+        "low_precision": lowp,
     }
     print(json.dumps(line), flush=True)
 

@@ -14,6 +14,7 @@
 
 #include "fa.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_fwd_mx.cuh"
 #include "fa_fwd_persist.cuh"
 #include "fa_fwd_stream.cuh"
 #include "fa_fwd_wide.cuh"
@@ -77,6 +78,16 @@ cudaError_t opt_in_smem_persist() {
   return cudaFuncSetAttribute(fa::fa_fwd_persist_kernel<D, true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               fa::PersistCfg<D, false>::kSmemBytes);
+}
+
+cudaError_t opt_in_smem_mx() {
+  cudaError_t e = cudaFuncSetAttribute(
+      fa::fa_fwd_mx_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      fa::MxCfg::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(fa::fa_fwd_mx_kernel<true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              fa::MxCfg::kSmemBytes);
 }
 
 template <int D, bool CAUSAL>
@@ -157,6 +168,7 @@ int device_ready(int** word_out, int* dev_out = nullptr) {
         opt_in_smem_stream<128>() != cudaSuccess ||
         opt_in_smem_stream<128, true>() != cudaSuccess ||
         opt_in_smem_persist<64>() != cudaSuccess ||
+        opt_in_smem_mx() != cudaSuccess ||
         opt_in_smem_persist<128>() != cudaSuccess ||
         opt_in_smem_wide<64, false>() != cudaSuccess ||
         opt_in_smem_wide<64, true>() != cudaSuccess ||
@@ -772,6 +784,59 @@ int fa_fwd_qk8(const void* q8, const void* k8, const void* v, void* o,
   return run_forward(q8, k8, v, o, lse, B, Hq, Hkv, Nq, Nkv, D, scale, causal,
                      nullptr, 0, true, static_cast<cudaStream_t>(stream),
                      true, q_descale, k_descale);
+}
+
+int fa_fwd_mxfp8(const void* q8, const void* k8, const void* v,
+                 const void* q_scale, const void* k_scale, void* o,
+                 float* lse, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                 float scale, int causal, void* stream) {
+  int st = check_args(q8, k8, v, o, lse, B, Hq, Hkv, Nq, Nkv, D, scale);
+  if (st != FA_OK) return st;
+  if (q_scale == nullptr || k_scale == nullptr) return FA_ERR_INVALID_VALUE;
+  if (D != 128) return FA_ERR_UNSUPPORTED;
+  if (!aligned(q_scale, 4) || !aligned(k_scale, 4)) return FA_ERR_MISALIGNED;
+  int* word = nullptr;
+  int dev = 0;
+  if ((st = device_ready(&word, &dev)) != FA_OK) return st;
+  fa::FwdParams p;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.Nq = Nq;
+  p.Nkv = Nkv;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) *
+                                    1.4426950408889634074);
+  p.status = word;
+  p.wait_limit_ns = kWaitLimitNs;
+  p.kv_splits = 1;
+  p.work = nullptr;
+  p.B = B;
+  p.stream_len = 0;
+  p.epoch = next_epoch();
+  fa::MxScales sf;
+  sf.q_sf = static_cast<const uint32_t*>(q_scale);
+  sf.k_sf = static_cast<const uint32_t*>(k_scale);
+  CUtensorMap tq, tk, tv, to;
+  if ((st = encode_bhnd_e4m3(&tq, q8, static_cast<long long>(B) * Hq, Nq,
+                             D)) ||
+      (st = encode_bhnd_e4m3(&tk, k8, static_cast<long long>(B) * Hkv, Nkv,
+                             D)) ||
+      (st = encode_bhnd(&tv, v, static_cast<long long>(B) * Hkv, Nkv, D,
+                        fa::kBN)) ||
+      (st = encode_bhnd(&to, o, static_cast<long long>(B) * Hq, Nq, D, 32)))
+    return st;
+  const dim3 grid((Nq + fa::kBM - 1) / fa::kBM, Hq, B);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (causal)
+    fa::fa_fwd_mx_kernel<true>
+        <<<grid, fa::kMxThreads, fa::MxCfg::kSmemBytes, s>>>(tq, tk, tv, to,
+                                                             p, sf);
+  else
+    fa::fa_fwd_mx_kernel<false>
+        <<<grid, fa::kMxThreads, fa::MxCfg::kSmemBytes, s>>>(tq, tk, tv, to,
+                                                             p, sf);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int D,

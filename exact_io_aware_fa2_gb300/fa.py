@@ -31,7 +31,8 @@ SYMBOLS = ("fa_fwd", "fa_fwd_ws", "fa_fwd_workspace_size", "fa_fwd_noalloc",
            "fa_fwd_qk8", "fa_fwd_schedule", "fa_set_schedule", "fa_fwd_host",
            "fa_probe_flag_wait", "fa_fwd_schedule_for",
            "fa_status_string", "fa_last_device_error",
-           "fa_probe_bounded_wait", "fa_version", "fa_tensor_map_encodes")
+           "fa_probe_bounded_wait", "fa_version", "fa_tensor_map_encodes",
+           "fa_fwd_mxfp8")
 
 _lib = None
 _lock = threading.Lock()
@@ -97,6 +98,9 @@ def load():
         lib.fa_fwd_schedule_for.argtypes = [ci] * 8 + [pi] * 4 + [
             ctypes.POINTER(ctypes.c_size_t)]
         lib.fa_fwd_schedule_for.restype = ci
+        lib.fa_fwd_mxfp8.argtypes = [vp] * 7 + [ci] * 6 + [ctypes.c_float,
+                                                           ci, vp]
+        lib.fa_fwd_mxfp8.restype = ci
         lib.fa_tensor_map_encodes.argtypes = []
         lib.fa_tensor_map_encodes.restype = ctypes.c_size_t
         _lib = lib
@@ -353,6 +357,62 @@ def fwd_qk8(q8, k8, v, scale=None, q_descale=1.0, k_descale=1.0,
         raise FAError(st)
     if check:
         _check_device_status(dev, "fa_fwd_qk8")
+    return out, lse
+
+
+def fwd_mxfp8_raw(q8_ptr, k8_ptr, v_ptr, qs_ptr, ks_ptr, o_ptr, lse_ptr, B,
+                  Hq, Hkv, Nq, Nkv, D, scale, causal, stream_handle):
+    """Direct call of ``fa_fwd_mxfp8``; returns the status."""
+    return int(load().fa_fwd_mxfp8(
+        *[ctypes.c_void_p(x) for x in (q8_ptr, k8_ptr, v_ptr, qs_ptr, ks_ptr,
+                                       o_ptr, lse_ptr)],
+        B, Hq, Hkv, Nq, Nkv, D, ctypes.c_float(scale), 1 if causal else 0,
+        ctypes.c_void_p(stream_handle)))
+
+
+def fwd_mxfp8(q8, k8, v, q_scale, k_scale, scale=None, causal=False,
+              out=None, lse=None, check=False):
+    """Forward with MXFP8 Q and K through ``fa_fwd_mxfp8``: e4m3 values
+    (``torch.float8_e4m3fn`` [B, H, N, D]) with one ue8m0 scale byte per 32
+    head-dim elements (``torch.uint8`` [B, H, N, D // 32]), and bf16 V; D
+    must be 128.  ``check`` as for ``fwd``."""
+    for name, t, dt in (("q8", q8, torch.float8_e4m3fn),
+                        ("k8", k8, torch.float8_e4m3fn),
+                        ("v", v, torch.bfloat16),
+                        ("q_scale", q_scale, torch.uint8),
+                        ("k_scale", k_scale, torch.uint8)):
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be 4-D")
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.device != q8.device or t.device.type != "cuda":
+            raise ValueError("all inputs must be CUDA tensors on one device")
+    B, Hq, Nq, D = q8.shape
+    if k8.shape != v.shape or k8.shape[0] != B or k8.shape[3] != D:
+        raise ValueError("k8, v must be [B, Hkv, Nkv, D] matching q8")
+    if D % 32 != 0 or q_scale.shape != (B, Hq, Nq, D // 32) or \
+            k_scale.shape != (B, k8.shape[1], k8.shape[2], D // 32):
+        raise ValueError("scales must be [B, H, N, D // 32] per operand")
+    Hkv, Nkv = k8.shape[1], k8.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dev = q8.device
+    if out is None:
+        out = torch.empty(B, Hq, Nq, D, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = fwd_mxfp8_raw(q8.data_ptr(), k8.data_ptr(), v.data_ptr(),
+                           q_scale.data_ptr(), k_scale.data_ptr(),
+                           out.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Nq,
+                           Nkv, D, scale, causal,
+                           torch.cuda.current_stream(dev).cuda_stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_mxfp8")
+    if check:
+        _check_device_status(dev, "fa_fwd_mxfp8")
     return out, lse
 
 

@@ -42,6 +42,9 @@ class Workload:
     k_spike_mult: float = 1.0
     # Q and K quantised per tensor to e4m3 (the fa_fwd_qk8 path)
     qk8: bool = False
+    # Q and K quantised to MXFP8: e4m3 with a power-of-two scale per 32
+    # head-dim elements (the fa_fwd_mxfp8 path)
+    mx: bool = False
 
     @property
     def scale(self):
@@ -92,6 +95,9 @@ WORKLOADS = {
         # The pages' shape with e4m3 Q and K (per-tensor descales).
         Workload("qk8_b1_h8_q4096_kv8192_d128", 1, 8, 8, 4096, 8192, 128,
                  False, qk8=True),
+        # The pages' shape with MXFP8 Q and K (a scale per 32 elements).
+        Workload("mxfp8_b1_h8_q4096_kv8192_d128", 1, 8, 8, 4096, 8192, 128,
+                 False, mx=True),
         # The pages' shape with 5 heads: 80 tile pairs fill 53% of the 152
         # SMs, so the stream schedule (equal K/V-block shares per CTA) runs
         # it.  Not one of the pages' shapes; it measures that schedule.
@@ -169,3 +175,51 @@ def make_qk8_inputs(B, Hq, Hkv, Nq, Nkv, D, seed=0, q_std=1.0):
     q8, qd = quantize_e4m3(q)
     k8, kd = quantize_e4m3(k)
     return q8, k8, v, qd, kd
+
+
+MX_BLOCK = 32
+E4M3_MIN_NORMAL_EXP = -6
+
+
+def quantize_mxfp8(t):
+    """MXFP8 quantisation of a [..., D] tensor along its last dimension: for
+    every block of 32 consecutive elements, the smallest power of two 2^e
+    with amax / 2^e <= 448 (e clamped to [-127, 127]; e = -127 for an
+    all-zero block) is the block's scale, stored as the ue8m0 byte e + 127,
+    and the elements become e4m3 values of t / 2^e (round to nearest; the
+    division is exact).  Returns (t8 float8_e4m3fn, scales uint8 [..., D/32]).
+    This is the input recipe of the MXFP8 path, not part of the method."""
+    x = t.float()
+    D = x.shape[-1]
+    if D % MX_BLOCK:
+        raise ValueError("last dimension must be a multiple of 32")
+    xb = x.reshape(*x.shape[:-1], D // MX_BLOCK, MX_BLOCK)
+    amax = xb.abs().amax(dim=-1)
+    e = torch.where(amax > 0, torch.ceil(torch.log2(amax / E4M3_MAX)),
+                    torch.full_like(amax, -127.0))
+    # log2 rounding can land one short of the bound: fix by one step
+    e = torch.where(amax / torch.exp2(e) > E4M3_MAX, e + 1, e)
+    e = e.clamp(-127, 127)
+    q8 = (xb / torch.exp2(e).unsqueeze(-1)).reshape(x.shape).to(
+        torch.float8_e4m3fn)
+    return q8, (e + 127).to(torch.uint8)
+
+
+def dequantize_mxfp8(t8, scales):
+    """The exact values an MXFP8 pair (e4m3 t8, ue8m0 scales) stands for,
+    in float64: t8 times 2^(byte - 127) per 32-element block."""
+    x = t8.to(torch.float64)
+    D = x.shape[-1]
+    s = torch.exp2(scales.to(torch.float64) - 127.0)
+    return (x.reshape(*x.shape[:-1], D // MX_BLOCK, MX_BLOCK) *
+            s.unsqueeze(-1)).reshape(x.shape)
+
+
+def make_mxfp8_inputs(B, Hq, Hkv, Nq, Nkv, D, seed=0, q_std=1.0):
+    """Seeded inputs of the MXFP8 path: the N(0,1) bf16 Q, K, V of
+    make_custom with Q and K quantised to MXFP8.  Returns
+    (q8, k8, v, q_scale, k_scale)."""
+    q, k, v = make_custom(B, Hq, Hkv, Nq, Nkv, D, seed=seed, q_std=q_std)
+    q8, qs = quantize_mxfp8(q)
+    k8, ks = quantize_mxfp8(k)
+    return q8, k8, v, qs, ks

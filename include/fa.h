@@ -165,6 +165,37 @@ int fa_fwd_qk8(const void* q8, const void* k8, const void* v, void* o,
                float scale, float q_descale, float k_descale, int causal,
                void* stream);
 
+/*
+ * fa_fwd_mxfp8 — fa_fwd with Q and K in MXFP8: 8-bit floating point (e4m3)
+ * with one power-of-two scale per 32 consecutive head-dim elements of a row.
+ *
+ * The block-scaled low-precision MMA that "Flash Attention на 5090 в CUDA
+ * C++" sets as its goal (introduction; "Что дальше": MXFP8/NVFP4 MMA), in
+ * its 8-bit form: S = Q K^T runs on the tensor cores as a block-scaled
+ * e4m3 x e4m3 product (tcgen05 kind::mxf8f6f4, one scale per 32 elements of
+ * each operand) with fp32 accumulation; P V stays bf16.  The scores are
+ *     S[i][j] = scale * sum_b 2^(qs[i][b] - 127) 2^(ks[j][b] - 127)
+ *                       * sum_{d = 32b .. 32b+31} q8[i][d] k8[j][d],
+ * the dot products of the exactly dequantised rows.
+ *
+ *   q8       device pointer, e4m3 (1 byte) [B, Hq,  Nq,  D], contiguous
+ *   k8       device pointer, e4m3 (1 byte) [B, Hkv, Nkv, D], contiguous
+ *   v, o, lse, B, Hq, Hkv, Nq, Nkv, scale, causal, stream: as for fa_fwd
+ *   q_scale  device pointer, ue8m0 bytes [B, Hq,  Nq,  D / 32], contiguous,
+ *            4-byte aligned: qs above (value 2^(byte - 127))
+ *   k_scale  device pointer, ue8m0 bytes [B, Hkv, Nkv, D / 32], likewise
+ *   D        must be 128 (FA_ERR_UNSUPPORTED otherwise)
+ *
+ * Runs one 128-row query tile per CTA (the scale factors live in tensor
+ * memory beside S and O), with no split-KV.  Ownership, validation,
+ * asynchrony and errors as fa_fwd; FA_ERR_INVALID_VALUE for a NULL scale
+ * pointer, FA_ERR_MISALIGNED for one not 4-byte aligned.
+ */
+int fa_fwd_mxfp8(const void* q8, const void* k8, const void* v,
+                 const void* q_scale, const void* k_scale, void* o,
+                 float* lse, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                 float scale, int causal, void* stream);
+
 /* Schedules reported by fa_fwd_schedule (and forced by fa_set_schedule). */
 enum {
     FA_SCHEDULE_AUTO = -1,    /* fa_set_schedule only: choose per shape    */

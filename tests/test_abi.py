@@ -205,3 +205,16 @@ def test_tensor_map_counter_needs_no_device(lib):
     """fa_tensor_map_encodes reads a host counter: callable without a GPU,
     and no failed call above encoded anything."""
     assert fa.tensor_map_encodes() == 0
+
+
+def test_mxfp8_entry_validates_before_the_device(lib):
+    """fa_fwd_mxfp8: a NULL scale pointer, a head dim other than 128 and a
+    misaligned scale pointer are refused on the host."""
+    vp = ctypes.c_void_p
+    args = lambda qs, ks, D: (vp(P), vp(P), vp(P), vp(qs), vp(ks), vp(P),
+                              vp(P), 1, 2, 1, 128, 128, D, ctypes.c_float(0.1),
+                              0, None)
+    assert lib.fa_fwd_mxfp8(*args(None, P, 128)) == 1
+    assert lib.fa_fwd_mxfp8(*args(P, None, 128)) == 1
+    assert lib.fa_fwd_mxfp8(*args(P, P, 64)) == 2
+    assert lib.fa_fwd_mxfp8(*args(P + 2, P, 128)) == 3
