@@ -605,7 +605,12 @@ def run_ours(args, w):
         peak_src += "; x4/3: QK^T at the e4m3 rate (2x bf16), PV at bf16"
     # A split-KV step is the forward kernel plus the merge; the step time
     # (both kernels) then stands for the forward kernel's, a lower bound.
-    sched = fa.schedule(w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D, w.causal)
+    if w.mx:
+        # fa_fwd_mxfp8 runs one 128-row query tile per CTA, never split
+        sched = {"kind": "one_tile", "ctas": w.B * w.Hq * -(-w.Nq // 128),
+                 "pieces": 1, "blocks_per_cta": 0}
+    else:
+        sched = fa.schedule(w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D, w.causal)
     split = sched["kind"] == "split_kv"
     launches_per_step = 2 if split else 1
 
