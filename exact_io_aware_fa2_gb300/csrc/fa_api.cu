@@ -557,9 +557,18 @@ template <int D>
 int launch_persist(const CUtensorMap& q, const CUtensorMap& k,
                    const CUtensorMap& v, const CUtensorMap& o,
                    const fa::FwdParams& p, int ctas, cudaStream_t stream) {
+  // The kernel's register split redistributes the launch allocation: the
+  // build must have given it kPersistRegsLaunch registers per thread.
+  static const bool regs_ok = [] {
+    cudaFuncAttributes a;
+    return cudaFuncGetAttributes(&a, fa::fa_fwd_persist_kernel<D, true>) ==
+               cudaSuccess &&
+           a.numRegs == fa::kPersistRegsLaunch;
+  }();
+  if (!regs_ok) return FA_ERR_CUDA;
   fa::fa_fwd_persist_kernel<D, true>
-      <<<ctas, fa::kThreads, fa::PersistCfg<D, false>::kSmemBytes, stream>>>(
-          q, k, v, o, p);
+      <<<ctas, fa::kPersistThreads, fa::PersistCfg<D, false>::kSmemBytes,
+         stream>>>(q, k, v, o, p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

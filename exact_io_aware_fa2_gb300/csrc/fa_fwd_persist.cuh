@@ -39,6 +39,24 @@
 
 namespace fa {
 
+// Warps: warpgroup 0 holds the MMA warp, the TMA warp and two idle warps,
+// warpgroups 1 and 2 the softmax of tiles A and B.  Warpgroup 0 gives up
+// registers and the softmax warpgroups take them: launched at
+// kPersistRegsLaunch per thread (384 threads, the most that fits), then
+// 128 x kPersistRegsLow + 256 x kPersistRegsHigh, the same total.  (At
+// head dim 64 this removed the softmax's spills: causal B4 H16 N2048 63.5 ->
+// 61.3 us; the same split in the one-pair-per-CTA kernel measured 1.8%
+// slower on the 4096 x 8192 shape and is not used there.)
+constexpr int kPersistThreads = 384;
+constexpr int kPersistSoftmaxWarp0 = 4;
+constexpr int kPersistRegsLaunch = 168;
+constexpr int kPersistRegsLow = 104;
+constexpr int kPersistRegsHigh = 200;
+static_assert(128 * kPersistRegsLow + 256 * kPersistRegsHigh ==
+                  kPersistThreads * kPersistRegsLaunch,
+              "register split");
+static_assert(kPersistRegsLaunch * kPersistThreads <= 65536, "launch");
+
 template <int D, bool QK8>
 struct PersistCfg {
   using C = FwdCfg<D, QK8>;
@@ -92,7 +110,7 @@ __device__ __forceinline__ PersistItem persist_decode(const FwdParams& p,
 }
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kPersistThreads, 1)
     fa_fwd_persist_kernel(const __grid_constant__ CUtensorMap tmQ,
                           const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV,
@@ -194,6 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{smem_addr(wstate)};
 
+  // Warpgroup 0 (TMA, MMA and two idle warps) gives registers back first;
+  // the softmax warpgroups' incs wait until they are free.
+  if (warp < kPersistSoftmaxWarp0) {
+  regs_dec<kPersistRegsLow>();
   if (warp == kLoadWarp) {
     // ============================ TMA producer ============================
     if (lane == 0) {
@@ -347,9 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Every MMA this warp issued completes before the CTA tears down.
     mma_commit_w(bDrain);
     mbar_wait(bDrain, 0, wc, false);
-  } else {
+  }
+  }  // warpgroup 0
+  else {
+    regs_inc<kPersistRegsHigh>();
     // ============================ softmax warps ===========================
-    const int x = (warp - kSoftmaxWarp0) >> 2;     // tile A (0) or B (1)
+    const int x = (warp - kPersistSoftmaxWarp0) >> 2;   // tile A (0) or B (1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float c = p.scale_log2;
     const bool neg_scale = c < 0.f;

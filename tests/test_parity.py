@@ -425,11 +425,35 @@ def test_check_option_reads_the_device_status():
 
 # ------------------------------------------------------ persistent schedule
 
+def test_persistent_d64_rescales_in_late_blocks():
+    """The persistent causal schedule at head dim 64 when a late block moves
+    a row's reference max, so O (in TMEM, with the previous P*V's result)
+    is rescaled mid-row: keys from 700 on are scaled by 6, so rows past 700
+    move their reference in a late block; whole heads against the
+    oracle."""
+    B, Hq, Hkv, N, D = 2, 48, 8, 1536, 64
+    q, k, v = make_custom(B, Hq, Hkv, N, N, D, seed=77, q_std=2.0)
+    k[:, :, 700:] *= 6.0
+    q, k, v = (t.cuda() for t in (q, k, v))
+    scale = 1.0 / math.sqrt(D)
+    assert fa.schedule(B, Hq, Hkv, N, N, D, True)["kind"] == "persist"
+    o, lse = fa.fwd(q, k, v, scale=scale, causal=True, check=True)
+    g = Hq // Hkv
+    for b, h in {(0, 0), (1, 17), (B - 1, Hq - 1)}:
+        O, L = oracle.attention_fp64(q[b:b + 1, h:h + 1].cpu(),
+                                     k[b:b + 1, h // g:h // g + 1].cpu(),
+                                     v[b:b + 1, h // g:h // g + 1].cpu(),
+                                     scale, True)
+        print(check(o[b:b + 1, h:h + 1].cpu(), lse[b:b + 1, h:h + 1].cpu(),
+                    O, L, f"persist rescale b{b} h{h}"))
+
+
 @pytest.mark.parametrize("B,Hq,Hkv,N,D", [
     (4, 16, 16, 2048, 64),      # 512 pairs: 3-4 pairs per CTA
     (2, 12, 4, 1000, 128),      # ragged tail tile, GQA
     (1, 3, 1, 300, 64),         # fewer pairs than SMs, tile B ragged
     (3, 50, 50, 640, 128),      # 450 pairs, pairs without a second tile
+    (2, 24, 6, 1100, 64),       # GQA; each head's last pair has no tile B
 ])
 def test_persistent_schedule_matches_one_cta_per_pair(B, Hq, Hkv, N, D):
     """Causal shapes run persistent CTAs over longest-first lists of tile
