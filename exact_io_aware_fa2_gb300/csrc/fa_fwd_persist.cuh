@@ -47,6 +47,19 @@ namespace fa {
 // head dim 64 this removed the softmax's spills: causal B4 H16 N2048 63.5 ->
 // 61.3 us; the same split in the one-pair-per-CTA kernel measured 1.8%
 // slower on the 4096 x 8192 shape and is not used there.)
+// Give up / take registers for the rest of the calling warpgroup's code:
+// every warp of the warpgroup executes the same call, and the registers the
+// incs take must not exceed what the decs gave back (the block's launch
+// allocation is fixed).
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 constexpr int kPersistThreads = 384;
 constexpr int kPersistSoftmaxWarp0 = 4;
 constexpr int kPersistRegsLaunch = 168;

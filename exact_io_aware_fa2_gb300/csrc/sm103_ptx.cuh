@@ -457,19 +457,6 @@ __device__ __forceinline__ void tmem_st_wait() {
 // ------------------------------------------------------------------ math
 
 // Hardware base-2 exponential (MUFU), flush-to-zero; ex2(-inf) = +0.
-// Give up / take registers for the rest of the calling warpgroup's code:
-// every warp of the warpgroup executes the same call, and the registers the
-// incs take must not exceed what the decs gave back (the block's launch
-// allocation is fixed).
-template <uint32_t N>
-__device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
