@@ -328,13 +328,25 @@ Plan plan_forward(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
     pl.persist_ctas = static_cast<int>(pairs < sms ? pairs : sms);
     return pl;
   }
-  if (pl.splits > 1 || !stream_ok) return pl;
+  if (!stream_ok) return pl;
   const int64_t pairs = static_cast<int64_t>(B) * Hq *
                         ((Nq + 2 * fa::kBM - 1) / (2 * fa::kBM));
+  bool from_split = false;
+  if (pl.splits > 1) {
+    // A split whose pieces need more than one wave of CTAs loses to the
+    // stream schedule, which gives every SM one equal share (measured on
+    // GB300, split against stream: 64 pairs x 16384 keys in 7 pieces, 448
+    // CTAs, 135.7 vs 111.6 us at D = 128 and 100.6 vs 90.2 at D = 64; 32
+    // pairs x 32768 keys in 9 pieces 209.4 vs 193.5; within one wave the
+    // split wins, e.g. 16 pairs x 16384 keys in 4 pieces 66.0 vs 72.2).
+    if (pairs * pl.splits <= sms) return pl;
+    pl.splits = 1;
+    from_split = true;
+  }
   const int64_t nbp = (Nkv + fa::kBN - 1) / fa::kBN;
   const int64_t total = pairs * nbp;
   const int64_t L = (total + sms - 1) / sms;
-  if (forced != FA_SCHEDULE_STREAM) {
+  if (forced != FA_SCHEDULE_STREAM && !from_split) {
     const int64_t waves = (pairs + sms - 1) / sms;
     const double plain = static_cast<double>(waves * nbp) +
                          kPairOverheadBlocks;

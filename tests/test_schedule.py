@@ -34,12 +34,21 @@ def sched(B, Hq, Hkv, Nq, Nkv, D, causal=False, sms=152):
     ((1, 5, 5, 4096, 4096, 128), "stream"),    # 80 pairs, 4096 keys
     ((1, 5, 5, 4096, 2048, 128), "plain"),     # short rows: overhead wins
     ((1, 5, 5, 4096, 8192, 64), "stream"),
+    # few pairs: split-KV while its pieces fit one wave, else stream
+    ((1, 4, 4, 2048, 16384, 128), "split_kv"),   # 16 pairs x 4 pieces
+    ((4, 8, 8, 512, 8192, 128), "split_kv"),     # 64 pairs x 2 pieces
+    ((2, 16, 16, 512, 16384, 128), "stream"),    # would be 7 x 64 CTAs
+    ((1, 16, 16, 1024, 16384, 64), "stream"),
+    ((2, 8, 8, 1024, 32768, 128), "stream"),
 ])
 def test_choices_measured_on_gb300(shape, kind):
     """The estimate picks the schedule measured faster on GB300 (stream
     against plain: 74 vs 99 us at 80 pairs, 95 vs 99 at 112, 156 vs 189 at
     200 pairs, 50 vs 55 with 4096 keys; plain: 99 vs 105 at 128 pairs, 101
-    vs 113 at 144, 33 vs 38 on 2048-key rows)."""
+    vs 113 at 144, 33 vs 38 on 2048-key rows; split against stream: 66 vs
+    72 us for 16 pairs of 16384 keys, 68 vs 71 for 64 pairs of 8192; stream
+    against a split of more than one wave: 112 vs 136 us for 64 pairs of
+    16384 keys, 89 vs 101 at D = 64, 194 vs 209 for 32 pairs of 32768)."""
     assert sched(*shape)["kind"] == kind
 
 
@@ -151,6 +160,9 @@ def test_invariants(sms):
                 assert s["pieces"] <= max(1, longest // 4), what
                 assert s["ctas"] == units * s["pieces"], what
                 assert units * 2 <= sms, what
+                # without a mask at head dims 64 and 128 a split takes at
+                # most one wave (else the stream schedule runs)
+                assert causal or D not in (64, 128) or s["ctas"] <= sms, what
                 slot = (rows * (D + 3)) * 4
                 assert s["workspace"] == units * s["pieces"] * slot, what
             else:
@@ -160,5 +172,7 @@ def test_invariants(sms):
                 L = s["blocks_per_cta"]
                 assert L == math.ceil(total / sms), what
                 assert s["ctas"] == math.ceil(total / L) <= sms, what
-                assert 2 * L >= nbp, what
+                # at least half a pair per CTA, unless the shape would
+                # otherwise split into more than one wave
+                assert 2 * L >= nbp or units * 2 <= sms, what
                 assert s["workspace"] == s["ctas"] * (SLOT[D] + 64) + 16, what
