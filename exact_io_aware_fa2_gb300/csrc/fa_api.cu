@@ -224,10 +224,16 @@ int device_ready(int** word_out, int* dev_out = nullptr) {
 // blocks each, at most kMaxSplits pieces).  The count minimises the
 // estimated time: waves of CTAs x (blocks per piece + kSplitOverheadBlocks,
 // a piece's fixed cost for its Q load, set-up and fp32 partial write, in
-// units of one K/V block), the smaller count on a tie.
+// units of one K/V block), the smaller count on a tie.  The one-tile kernel's
+// 64-key blocks are short against its fixed cost per piece: fitted to GB300
+// timings at head dims 192 and 256 (one wave of 2 to 4 pieces against 2 to
+// 3 waves of 7 to 9: 64 heads of 1024 x 8192 at D 192 62.5 vs 79.8 us,
+// 16 heads of 256 x 16384 at D 256 90.6 vs 100.8; 2 heads of 4096 x 32768
+// at D 256 266.1 vs 250.8 the other way), about 15 blocks.
 constexpr int kMinSplitBlocks = 4;
 constexpr int kMaxSplits = 64;
 constexpr int kSplitOverheadBlocks = 3;
+constexpr int kSplitOverheadBlocksOneTile = 15;
 
 // Query rows per CTA and keys per K/V block of the kernel a head dim runs
 // (the two-tile kernel: 256 and 128; the wide-head kernel: 128 and 64).
@@ -255,7 +261,9 @@ int plan_splits(int B, int Hq, int Nq, int Nkv, int D, int causal, int sms) {
   for (long long s = 1; s <= cap; ++s) {
     const long long waves = (ctas * s + sms - 1) / sms;
     const long long cost =
-        waves * ((longest + s - 1) / s + kSplitOverheadBlocks);
+        waves * ((longest + s - 1) / s +
+                 (keys_b == fa::kBN ? kSplitOverheadBlocks
+                                    : kSplitOverheadBlocksOneTile));
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best_s = s;
