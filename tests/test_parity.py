@@ -36,8 +36,11 @@ def check(o, lse, O, L, what=""):
     assert torch.isfinite(lse).all(), f"{what}: non-finite LSE"
     dO = (o.double() - O).abs()
     dL = (lse.double() - L).abs()
+    # the part no bf16 output can avoid: the oracle's own O rounded to bf16
+    floor = (O.to(torch.bfloat16).double() - O).abs().max()
     msg = (f"{what}: max|dO|={dO.max():.3e} mean|dO|={dO.mean():.3e} "
-           f"max|dLSE|={dL.max():.3e}")
+           f"max|dLSE|={dL.max():.3e} (oracle O rounded to bf16: max "
+           f"{floor:.3e})")
     assert dO.max() <= MAX_DO, msg
     assert dO.mean() <= MEAN_DO, msg
     assert dL.max() <= MAX_DLSE, msg
