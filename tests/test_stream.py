@@ -199,3 +199,28 @@ def test_forced_plain_disables_split_and_stream():
         print(_check(o.cpu(), lse.cpu(), O, L, "forced plain"))
     finally:
         fa.set_schedule("auto")
+
+
+@pytest.mark.parametrize("shape", [(2, 32, 8, 256, 16384, 128),
+                                   (2, 16, 4, 512, 16384, 64)])
+def test_auto_stream_in_place_of_multiwave_split(shape):
+    """Grouped-query shapes with few tile pairs whose split-KV pieces would
+    need more than one wave run the stream schedule by themselves (no forced
+    setting): packed GQA heads, 54 blocks per CTA; sampled heads against the
+    oracle."""
+    _needs_gb300_sm_count()
+    B, Hq, Hkv, Nq, Nkv, D = shape
+    assert fa.schedule(B, Hq, Hkv, Nq, Nkv, D, False)["kind"] == "stream"
+    q, k, v = make_custom(B, Hq, Hkv, Nq, Nkv, D, seed=Nq + Hq)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = fa.fwd(q.cuda(), k.cuda(), v.cuda(), scale=scale, causal=False,
+                    check=True)
+    o, lse = o.cpu(), lse.cpu()
+    g = Hq // Hkv
+    for b, h in {(0, 0), (0, g), (B - 1, Hq - 1)}:
+        O, L = oracle.attention_fp64(q[b:b + 1, h:h + 1],
+                                     k[b:b + 1, h // g:h // g + 1],
+                                     v[b:b + 1, h // g:h // g + 1], scale,
+                                     False)
+        print(_check(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], O, L,
+                     f"auto stream {shape} b{b} h{h}"))
