@@ -84,17 +84,14 @@ __device__ __forceinline__ StreamRange stream_range(const FwdParams& p,
 
 // Segment si (0 = the range's last pair, counting down).
 //
-// Block order within a segment: every CTA starts at the same time and
-// advances one block per step, so step t of every CTA runs at about the same
-// moment.  The plain schedule has all CTAs of a head load block t at step t,
-// which lets the L2 serve near-simultaneous requests for the same K/V lines
-// together.  Here the segment that starts at step t0 visits its blocks
-// [j0, j0 + n) rotated so that, wherever its range allows, the block at step
-// t is block t mod nbp, as in the plain schedule.  (On the 4096 x 8192
-// shape without the rotation, ncu counted twice the plain schedule's L2
-// read sectors.  The rotation did not change the time per block, which is
-// set by the kernel's loops: 1.48 us against the plain kernel's 1.42 us
-// with or without it.)
+// Block order within a segment: its blocks [j0, j0 + n) in order.  (Rotating
+// each segment so that step t of every CTA visits block t mod nbp, as the
+// one-pair-per-CTA grid does, was measured on GB300: the same time per
+// block and per launch, but when the call's K/V exceed what L2 keeps it
+// reads them about twice from DRAM, since a CTA whose run covers more than
+// one pair's blocks meets the same block again a whole pair later: 218 MB
+// against 138 MB read per launch for 25 heads of 2048 x 8192 at D 128,
+// where Q, K and V are 118 MB.)
 __device__ __forceinline__ StreamSeg stream_segment(const FwdParams& p,
                                                     const StreamRange& r,
                                                     int n_pairs, int nbp,
@@ -102,12 +99,10 @@ __device__ __forceinline__ StreamSeg stream_segment(const FwdParams& p,
   const int64_t g = (r.end - 1) / nbp - si;
   const int64_t s = max(r.start, g * nbp) - g * nbp;
   const int64_t e = min(r.end, (g + 1) * nbp) - g * nbp;
-  // steps of this CTA before this segment: its items in later pairs
-  const int64_t t0 = max(int64_t{0}, r.end - (g + 1) * nbp);
   StreamSeg sg;
   sg.j0 = static_cast<int>(s);
   sg.n = static_cast<int>(e - s);
-  sg.first = static_cast<int>(s + (((t0 - s) % (e - s)) + (e - s)) % (e - s));
+  sg.first = static_cast<int>(s);
   sg.kind = e < nbp ? kSegWriter : (s > 0 ? kSegMerger : kSegWhole);
   sg.first_cta = static_cast<int>((g * nbp) / p.stream_len);
   sg.pair = static_cast<int>(g % n_pairs);
