@@ -333,8 +333,11 @@ Plan plan_forward(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
   if (pl.splits == 1 && persist_ok(B, Hkv, Nkv, D, causal, qk8)) {
     const int64_t pairs = static_cast<int64_t>(B) * Hq *
                           ((Nq + 2 * fa::kBM - 1) / (2 * fa::kBM));
-    pl.persist_ctas = static_cast<int>(pairs < sms ? pairs : sms);
-    return pl;
+    // (the kernel numbers its list of pairs with 32-bit integers)
+    if (pairs < (int64_t{1} << 31)) {
+      pl.persist_ctas = static_cast<int>(pairs < sms ? pairs : sms);
+      return pl;
+    }
   }
   if (!stream_ok) return pl;
   const int64_t pairs = static_cast<int64_t>(B) * Hq *
@@ -586,6 +589,7 @@ int launch_persist(const CUtensorMap& q, const CUtensorMap& k,
            a.numRegs == fa::kPersistRegsLaunch;
   }();
   if (!regs_ok) return FA_ERR_CUDA;
+  if (p.scale_log2 == 0.f) return FA_ERR_INVALID_VALUE;  // see run_forward
   fa::fa_fwd_persist_kernel<D, true>
       <<<ctas, fa::kPersistThreads, fa::PersistCfg<D, false>::kSmemBytes,
          stream>>>(q, k, v, o, p);
@@ -716,8 +720,10 @@ int run_forward(const void* q, const void* k, const void* v, void* o,
       (qk8 ? static_cast<double>(q_descale) * k_descale : 1.0));
   p.status = word;
   p.wait_limit_ns = kWaitLimitNs;
-  const Plan pl =
-      plan_forward(B, Hq, Hkv, Nq, Nkv, D, causal, g_sm_count[dev], qk8);
+  Plan pl = plan_forward(B, Hq, Hkv, Nq, Nkv, D, causal, g_sm_count[dev], qk8);
+  // The persistent kernel hides masked keys through their scores, which
+  // needs a nonzero scale: a zero scale runs the one-pair-per-CTA kernels.
+  if (pl.persist_ctas > 0 && p.scale_log2 == 0.f) pl.persist_ctas = 0;
   p.kv_splits = pl.splits;
   p.work = nullptr;
   p.B = B;

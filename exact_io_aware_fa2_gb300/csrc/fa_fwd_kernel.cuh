@@ -277,15 +277,19 @@ __device__ __forceinline__ float top_rounding(float s_ext, float c,
 // visible up to Nkv and, when CAUSAL, up to the row's own index q_abs.
 // Steps: "Hacker News Digest — gpu-computing", section "v1 — базовая
 // версия", item 3 (running max and denominator); the lazy rescale is the
-// one-pass form of the same recurrence with a stale reference.
-template <int D, bool CAUSAL>
+// one-pass form of the same recurrence with a stale reference.  INTERIOR:
+// no key of the block needs masking here (every key is visible to every row
+// of the tile, or the hidden ones already hold the extreme's identity as
+// their score, see hide_keys), and no mask code is compiled.
+template <int D, bool CAUSAL, bool INTERIOR = false>
 __device__ __forceinline__ void softmax_block(
     uint32_t s_addr, uint32_t p_addr, uint32_t o_addr, int col0, int my_row0,
     int q_abs, int Nkv, float c, bool neg_scale, bool o_live, float& m_ref,
     float& l_run, float& w_run) {
   uint32_t sr[kBN];
   const bool need_mask =
-      (col0 + kBN > Nkv) || (CAUSAL && col0 + kBN - 1 > my_row0);
+      !INTERIOR &&
+      ((col0 + kBN > Nkv) || (CAUSAL && col0 + kBN - 1 > my_row0));
   // Unmasked blocks take the row's extreme from reducing TMEM loads (one
   // max/min per 32 columns, computed by the load itself).
   float red[kBN / 32];
@@ -367,6 +371,39 @@ __device__ __forceinline__ void softmax_block(
   tmem_st32(p_addr + 32, pp + 32);
   tmem_st_wait();
   tc_fence_before();
+}
+
+// Hide the keys n_vis .. kBN-1 of this block from this thread's row: their
+// scores in TMEM (the warp's 32 lanes at s_addr, kBN fp32 columns) become
+// idn, the identity of the row extreme (-inf, or +inf for a negative scale)
+// and a score whose weight exp2(idn * c - m) is 0 for any nonzero scale c.
+// The unmasked softmax_block then gives this block the same bits as the
+// masked one.  Chunks of 32 keys that every lane of the warp sees are left
+// alone, chunks that no lane sees are overwritten whole, and the chunks in
+// between are read, masked key by key and written back.  Returns once the
+// stores are complete.
+__device__ __forceinline__ void hide_keys(uint32_t s_addr, int n_vis,
+                                          float idn) {
+  const int lo = __reduce_min_sync(0xffffffffu, n_vis);  // all lanes see < lo
+  const int hi = __reduce_max_sync(0xffffffffu, n_vis);  // no lane sees >= hi
+  const uint32_t idn_b = __float_as_uint(idn);
+#pragma unroll 1
+  for (int cc = lo >> 5; cc < kBN / 32; ++cc) {
+    uint32_t v[32];
+    if (cc * 32 >= hi) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) v[k] = idn_b;
+    } else {
+      tmem_ld32(s_addr + cc * 32, v);
+      tmem_ld_wait();
+      reg_fence32(v);
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        if (cc * 32 + k >= n_vis) v[k] = idn_b;
+    }
+    tmem_st32(s_addr + cc * 32, v);
+  }
+  tmem_st_wait();
 }
 
 // Where a warp's finished rows go.  smem == 0: each lane stores its own row

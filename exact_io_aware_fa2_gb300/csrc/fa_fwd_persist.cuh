@@ -26,6 +26,11 @@
 //     pair's first S MMAs do not wait for any epilogue (at head dim 128 P
 //     lives in S's columns, whose last reader is the last P*V; at head dim 64
 //     P has its own columns).
+//   * Masking: only a tile's last block can hold hidden keys (its causal
+//     diagonal, or the end of the keys).  Their scores are overwritten in
+//     TMEM (hide_keys) and every block runs the same unmasked block code;
+//     the host sends calls with a zero scale, for which no score has weight
+//     0, to the one-pair-per-CTA kernels.
 //
 // Source of the method: as fa_fwd_kernel.cuh ("Hacker News Digest —
 // gpu-computing", section "Алгоритм Flash Attention 2", and the online
@@ -88,19 +93,19 @@ struct PersistCfg {
 };
 
 // Item (pair of the sorted list) that CTA c of G handles in its round r, or
-// -1 when that round has none for it.
-__device__ __forceinline__ int64_t persist_item(int64_t total, int G, int c,
-                                                int r) {
-  const int64_t i = static_cast<int64_t>(r) * G + ((r & 1) ? G - 1 - c : c);
+// -1 when that round has none for it.  The list has fewer than 2^31 items
+// (the host launches this kernel only then), so 32-bit arithmetic suffices.
+__device__ __forceinline__ int persist_item(int total, int G, int c, int r) {
+  const int i = r * G + ((r & 1) ? G - 1 - c : c);
   return i < total ? i : -1;
 }
 
 // Rounds of CTA c: items r with persist_item(...) >= 0 for r = 0 .. n-1.
-__device__ __forceinline__ int persist_rounds(int64_t total, int G, int c) {
-  const int64_t full = total / G;
-  const int64_t rem = total - full * G;
+__device__ __forceinline__ int persist_rounds(int total, int G, int c) {
+  const int full = total / G;
+  const int rem = total - full * G;
   const int pos = (full & 1) ? G - 1 - c : c;
-  return static_cast<int>(full) + (pos < rem ? 1 : 0);
+  return full + (pos < rem ? 1 : 0);
 }
 
 struct PersistItem {
@@ -108,17 +113,18 @@ struct PersistItem {
 };
 
 // Item i of the list: pairs longest first (for a causal mask the pair with
-// the highest index is the longest), then (batch, head).
+// the highest index is the longest), then (batch, head).  i = -1 (no item)
+// gives a harmless value that no caller uses.
 __device__ __forceinline__ PersistItem persist_decode(const FwdParams& p,
-                                                      int n_pairs,
-                                                      int64_t i) {
-  const int64_t bh_count = static_cast<int64_t>(p.B) * p.Hq;
-  const int64_t rank = i / bh_count;
-  const int64_t bh = i - rank * bh_count;
+                                                      int n_pairs, int i) {
+  const unsigned bh_count = static_cast<unsigned>(p.B * p.Hq);
+  const unsigned ui = static_cast<unsigned>(max(i, 0));
+  const unsigned rank = ui / bh_count;
+  const unsigned bh = ui - rank * bh_count;
   PersistItem it;
   it.pair = n_pairs - 1 - static_cast<int>(rank);
-  it.b = static_cast<int>(bh / p.Hq);
-  it.hq = static_cast<int>(bh - static_cast<int64_t>(it.b) * p.Hq);
+  it.b = static_cast<int>(bh / static_cast<unsigned>(p.Hq));
+  it.hq = static_cast<int>(bh) - it.b * p.Hq;
   return it;
 }
 
@@ -141,7 +147,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
   const int lane = threadIdx.x & 31;
 
   const int n_pairs = (p.Nq + 2 * kBM - 1) / (2 * kBM);
-  const int64_t total = static_cast<int64_t>(p.B) * p.Hq * n_pairs;
+  const int total = p.B * p.Hq * n_pairs;
   const int G = static_cast<int>(gridDim.x);
   const int cta = static_cast<int>(blockIdx.x);
   const int rounds = persist_rounds(total, G, cta);
@@ -240,8 +246,10 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
       int k_issued = 0, v_issued = 0, q_loads = 0;
       int sk = 0, kph = 0, sv = 0, vph = 0;
       bool ok = true;
+      Unit nxt = unit(0);
       for (int r = 0; ok && r < rounds; ++r) {
-        const Unit u = unit(r);
+        const Unit u = nxt;
+        if (r + 1 < rounds) nxt = unit(r + 1);
         const int zq = u.it.b * p.Hq + u.it.hq;
         const int zk = u.it.b * p.Hkv + u.it.hq / (p.Hq / p.Hkv);
         const int qb = r % NQ;
@@ -261,11 +269,10 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
         // With one Q buffer, the next pair's Q goes to L2 now, so its load
         // after this pair's last S is short.
         if (NQ == 1 && r + 1 < rounds) {
-          const Unit un = unit(r + 1);
-          const int zqn = un.it.b * p.Hq + un.it.hq;
-          for (int x = 0; x < (un.row0[1] < p.Nq ? 2 : 1); ++x)
+          const int zqn = nxt.it.b * p.Hq + nxt.it.hq;
+          for (int x = 0; x < (nxt.row0[1] < p.Nq ? 2 : 1); ++x)
             for (int c = 0; c < C::kQKBoxes; ++c)
-              tma_prefetch_l2_3d(&tmQ, c * C::kQKBoxCols, un.row0[x], zqn);
+              tma_prefetch_l2_3d(&tmQ, c * C::kQKBoxCols, nxt.row0[x], zqn);
         }
         for (int j = 0; j < u.n_pair; ++j) {
           if (!(ok = mbar_wait(bKEmpty(sk), kph ^ 1, wc))) break;
@@ -312,8 +319,11 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
     int ks = 0, kph = 0;      // stage and phase of the next K block
     int vs = 0, vph = 0;      // stage and phase of the next V block
     uint32_t pph = 0;         // bit x: phase of tile x's next P
+    // The next round's pair is worked out while this round's last P's are
+    // awaited, off the path from the last P to the next S.
+    Unit nxt = unit(0);
     for (int r = 0; ok && r < rounds; ++r) {
-      const Unit u = unit(r);
+      const Unit u = nxt;
       const int qb = r % NQ;
       if (!(ok = __all_sync(kAll, mbar_wait(bQFull(qb), (r / NQ) & 1, wc))))
         break;
@@ -357,7 +367,10 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
         }
         if (!ok) break;
         // Q of this pair is read by no later MMA
-        if (j == u.n_pair - 1) mma_commit_w(bQEmpty(qb));
+        if (j == u.n_pair - 1) {
+          mma_commit_w(bQEmpty(qb));
+          if (r + 1 < rounds) nxt = unit(r + 1);
+        }
         if (j < u.n_pair) {
           mma_commit_w(bKEmpty(ks));
           if (++ks == NK) {
@@ -393,31 +406,50 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
     const bool neg_scale = c < 0.f;
     uint32_t sph = 0;          // phase of this tile's next S
     bool ok = true;
+    // This round's rows, block count and (batch, head); the next round's
+    // are worked out while this round's last P*V runs.
+    int nx_row0, nx_nb;
+    PersistItem nx_it;
+    auto next_unit = [&](int r) {
+      const Unit u = unit(r);
+      nx_row0 = x ? u.row0[1] : u.row0[0];
+      nx_nb = x ? u.nblk[1] : u.nblk[0];
+      nx_it = u.it;
+    };
+    next_unit(0);
     for (int r = 0; r < rounds; ++r) {
-      int my_row0, nb;
-      PersistItem it;
-      {
-        const Unit u = unit(r);
-        my_row0 = x ? u.row0[1] : u.row0[0];
-        nb = x ? u.nblk[1] : u.nblk[0];
-        it = u.it;
-      }
+      const int my_row0 = nx_row0, nb = nx_nb;
+      const PersistItem it = nx_it;
       const int q_abs = my_row0 + (warp & 3) * 32 + lane;
       float m_ref = -INFINITY;   // reference max (log2 domain) of p and l
       float l_run = 0.f;         // sum of exp2(s*c - m_ref) over seen keys
       float w_run = 0.f;         // the divisor of O (see top_rounding)
+      const uint32_t s_at = tmem + lane_off + C::col_s(x);
+      const uint32_t p_at = tmem + lane_off + C::col_p(x);
+      const uint32_t o_at = tmem + lane_off + C::col_o(x);
+      // Only a tile's last block can hold hidden keys (the causal diagonal,
+      // or the end of the keys).  Their scores are overwritten in TMEM
+      // (hide_keys, which needs the nonzero scale the host guarantees), so
+      // every block runs the same unmasked code.
       for (int j = 0; ok && j < nb; ++j) {
         if (!(ok = __all_sync(kAll, mbar_wait(bSFull(x), sph, wc)))) break;
         sph ^= 1u;
         tc_fence_after();
-        softmax_block<D, CAUSAL>(tmem + lane_off + C::col_s(x),
-                                 tmem + lane_off + C::col_p(x),
-                                 tmem + lane_off + C::col_o(x), j * kBN,
-                                 my_row0, q_abs, p.Nkv, c, neg_scale, j >= 1,
-                                 m_ref, l_run, w_run);
+        const int col0 = j * kBN;
+        if (j + 1 == nb && (col0 + kBN > p.Nkv ||
+                            (CAUSAL && col0 + kBN - 1 > my_row0))) {
+          int lim = p.Nkv - col0;
+          if (CAUSAL) lim = min(lim, q_abs - col0 + 1);
+          hide_keys(s_at, max(0, min(kBN, lim)),
+                    neg_scale ? INFINITY : -INFINITY);
+        }
+        softmax_block<D, CAUSAL, true>(s_at, p_at, o_at, col0, my_row0, q_abs,
+                                       p.Nkv, c, neg_scale, j >= 1, m_ref,
+                                       l_run, w_run);
         __syncwarp();
         if (lane == 0) mbar_arrive(bPFull(x));
       }
+      if (r + 1 < rounds) next_unit(r + 1);
       // ---- epilogue of tile x: every warp of the tile waits for its O,
       // also when the tile is absent from this pair, so its O-empty
       // arrival stays in step with the MMA warp's rounds ----

@@ -209,7 +209,8 @@ enum {
 /*
  * fa_fwd_schedule — how fa_fwd, fa_fwd_ws, fa_fwd_qk8 and fa_fwd_noalloc run
  * this shape on the current device (the choice depends only on the shape
- * and the device's SM count).
+ * and the device's SM count, for any nonzero scale: a call whose scale is 0
+ * runs FA_SCHEDULE_PLAIN where this reports FA_SCHEDULE_PERSIST).
  *
  *   *kind            FA_SCHEDULE_PLAIN: one CTA per unit of query rows (a
  *                    pair of 128-row tiles; one tile for D 192/256 and for
@@ -227,7 +228,8 @@ enum {
  *                    order; a wait that runs out reports FA_ERR_TIMEOUT
  *                    through fa_last_device_error.
  *                    FA_SCHEDULE_PERSIST (causal mask, D 64 or 128, bf16
- *                    Q/K, no split, K and V of the call within 96 MiB):
+ *                    Q/K, no split, K and V of the call within 96 MiB,
+ *                    fewer than 2^31 pairs of query tiles):
  *                    at most one CTA per SM, each walking a list of whole
  *                    pairs of 128-row query tiles, longest first and dealt
  *                    out in a snake order, so short causal pairs share a

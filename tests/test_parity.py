@@ -485,3 +485,62 @@ def test_persistent_schedule_matches_one_cta_per_pair(B, Hq, Hkv, N, D):
                                      scale, True)
         print(check(o1[b:b + 1, h:h + 1].cpu(), l1[b:b + 1, h:h + 1].cpu(),
                     O, L, f"persist B{B} H{Hq}/{Hkv} N{N} D{D} b{b} h{h}"))
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nkv,D,scale", [
+    (2, 8, 2, 1000, 700, 128, None),     # rows past the keys: end-of-keys tail
+    (1, 4, 4, 640, 1300, 128, None),     # more keys than rows
+    (2, 6, 3, 777, 777, 128, -0.09),     # negative scale: +inf hides a key
+    (2, 10, 5, 1000, 1100, 64, 1.7),     # large scale at head dim 64
+])
+def test_persistent_hidden_keys_match_masked_path(B, Hq, Hkv, Nq, Nkv, D,
+                                                  scale):
+    """The persistent kernel hides a tile's masked keys by overwriting their
+    scores in TMEM with the row extreme's identity and then runs the
+    unmasked block code; the one-pair-per-CTA kernel masks key by key.  At
+    head dim 128 both are the two-tile kernel's arithmetic, so the results
+    agree bit for bit; at 64 (whose plain schedule is the one-tile kernel)
+    both match the oracle on whole heads."""
+    q, k, v = (t.cuda() for t in make_custom(B, Hq, Hkv, Nq, Nkv, D,
+                                             seed=Nq * 7 + Nkv))
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    assert fa.schedule(B, Hq, Hkv, Nq, Nkv, D, True)["kind"] == "persist"
+    o1, l1 = fa.fwd(q, k, v, scale=scale, causal=True)
+    try:
+        fa.set_schedule("plain")
+        o2, l2 = fa.fwd(q, k, v, scale=scale, causal=True)
+    finally:
+        fa.set_schedule("auto")
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+    if D == 128:
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    g = Hq // Hkv
+    for b, h in {(0, 0), (B - 1, Hq - 1)}:
+        O, L = oracle.attention_fp64(q[b:b + 1, h:h + 1].cpu(),
+                                     k[b:b + 1, h // g:h // g + 1].cpu(),
+                                     v[b:b + 1, h // g:h // g + 1].cpu(),
+                                     scale, True)
+        print(check(o1[b:b + 1, h:h + 1].cpu(), l1[b:b + 1, h:h + 1].cpu(),
+                    O, L, f"hidden keys B{B} H{Hq}/{Hkv} {Nq}x{Nkv} D{D}"))
+
+
+def test_zero_scale_on_a_persistent_shape():
+    """A zero scale leaves no score whose weight is 0, so a shape planned
+    for the persistent kernel runs the one-pair-per-CTA kernel instead:
+    every visible key gets weight 1, O is the mean of the visible V rows,
+    and the result equals the plain schedule's bit for bit."""
+    q, k, v = (t.cuda() for t in make_custom(2, 4, 2, 512, 512, 128, seed=9))
+    assert fa.schedule(2, 4, 2, 512, 512, 128, True)["kind"] == "persist"
+    o1, l1 = fa.fwd(q, k, v, scale=0.0, causal=True, check=True)
+    try:
+        fa.set_schedule("plain")
+        o2, l2 = fa.fwd(q, k, v, scale=0.0, causal=True, check=True)
+    finally:
+        fa.set_schedule("auto")
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    n = torch.arange(1, 513, dtype=torch.float64)
+    assert torch.allclose(l1[1, 3].double().cpu(), n.log(), atol=1e-4)
+    O, L = oracle.attention_fp64(q[1:2, 3:4].cpu(), k[1:2, 1:2].cpu(),
+                                 v[1:2, 1:2].cpu(), 0.0, True)
+    print(check(o1[1:2, 3:4].cpu(), l1[1:2, 3:4].cpu(), O, L, "scale 0"))
