@@ -276,22 +276,25 @@ int plan_splits(int B, int Hq, int Nq, int Nkv, int D, int causal, int sms) {
 // when whole tile pairs leave SMs idle in their last wave, give every CTA
 // an equal contiguous share of all (pair, K/V block) items instead.  Costs
 // in units of one K/V block of one pair on the two-tile kernel, fitted to
-// GB300 timings of both schedules (D = 128; 80 to 256 pairs; 2048, 4096 and
-// 8192 keys; D = 64 checked):
-//   plain  = waves x blocks per pair + kPairOverheadBlocks
-//   stream = kStreamBlockFactor x blocks per CTA + kStreamOverheadBlocks
-//            + kSegmentBlocks x (segments per CTA - 1)
-// (the stream kernel's blocks are 9% slower, and its partial writes,
-// merges and segment switches cost about 9 blocks more than the plain
-// kernel's start-up and epilogue).  Stream runs when estimated at least
-// kStreamGain faster and a CTA's share is at least half a pair (a merger
-// then combines at most two partials).  Measured, stream against plain:
-// 80 pairs 74.4 vs 98.9 us, 112 pairs 94.8 vs 99.0, 200 pairs 156.3 vs
-// 189.1; plain wins at 128 pairs (99.0 vs 105.1) and on 2048-key rows.
-constexpr double kPairOverheadBlocks = 6.2;
-constexpr double kStreamBlockFactor = 1.09;
-constexpr double kStreamOverheadBlocks = 13.2;
-constexpr double kSegmentBlocks = 2.5;
+// GB300 timings of both schedules:
+//   plain  = waves x blocks per pair + pair_overhead
+//   stream = block_factor x blocks per CTA + stream_overhead
+//            + segment_cost x (segments per CTA - 1)
+// At D = 128 (80 to 256 pairs; 2048, 4096 and 8192 keys) the stream
+// kernel's blocks are 9% slower and its partial writes, merges and segment
+// switches cost about 9 blocks more than the plain kernel's start-up and
+// epilogue; at D = 64 (22 shapes of 32 to 256 pairs and 4096 to 32768
+// keys, least squares) its blocks are as fast and the rest costs about 9
+// blocks more.  Stream runs when estimated at least kStreamGain faster and
+// a CTA's share is at least half a pair (a merger then combines at most
+// two partials).  Measured, stream against plain at D = 128: 80 pairs 71.7
+// vs 98.3 us, 112 pairs 89.2 vs 98.5, 200 pairs 148.8 vs 192.5, 128 pairs
+// 100.5 vs 100.4 (plain kept); at D = 64 and 128 pairs 83.2 vs 90.1.
+struct StreamCost {
+  double pair_overhead, block_factor, stream_overhead, segment_cost;
+};
+constexpr StreamCost kStreamCostD128{6.2, 1.09, 13.2, 2.5};
+constexpr StreamCost kStreamCostD64{8.8, 0.98, 17.4, 0.0};
 constexpr double kStreamGain = 0.98;
 
 // Schedule forced by fa_set_schedule (FA_SCHEDULE_AUTO: the estimate).
@@ -356,15 +359,17 @@ Plan plan_forward(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
   }
   const int64_t nbp = (Nkv + fa::kBN - 1) / fa::kBN;
   const int64_t total = pairs * nbp;
+  // (the kernel numbers its items with 32-bit integers)
+  if (total >= (int64_t{1} << 31)) return pl;
   const int64_t L = (total + sms - 1) / sms;
   if (forced != FA_SCHEDULE_STREAM && !from_split) {
+    const StreamCost& k = D == 64 ? kStreamCostD64 : kStreamCostD128;
     const int64_t waves = (pairs + sms - 1) / sms;
-    const double plain = static_cast<double>(waves * nbp) +
-                         kPairOverheadBlocks;
+    const double plain = static_cast<double>(waves * nbp) + k.pair_overhead;
     const int64_t segments = (L - 1 + nbp - 1) / nbp + 1;   // at most
-    const double stream = kStreamBlockFactor * static_cast<double>(L) +
-                          kStreamOverheadBlocks +
-                          kSegmentBlocks * static_cast<double>(segments - 1);
+    const double stream = k.block_factor * static_cast<double>(L) +
+                          k.stream_overhead +
+                          k.segment_cost * static_cast<double>(segments - 1);
     if (2 * L < nbp || stream > kStreamGain * plain) return pl;
   }
   pl.stream_len = static_cast<int>(L);

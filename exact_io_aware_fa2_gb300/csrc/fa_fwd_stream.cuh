@@ -64,21 +64,22 @@ struct StreamSeg {
 };
 
 // Segments of this CTA's range: [start, end) of the g-major item sequence.
+// The host runs this schedule only for fewer than 2^31 items, so item
+// indices and every quotient below fit 32-bit integers (whose divisions
+// cost a fraction of 64-bit ones, on the path between segments).
 struct StreamRange {
-  int64_t start, end;
+  int start, end;
   int n_seg;
 };
 
 __device__ __forceinline__ StreamRange stream_range(const FwdParams& p,
                                                     int n_pairs, int nbp,
                                                     int cta) {
-  const int64_t total = static_cast<int64_t>(p.B) * p.Hq * n_pairs * nbp;
+  const int total = p.B * p.Hq * n_pairs * nbp;
   StreamRange r;
-  r.start = static_cast<int64_t>(cta) * p.stream_len;
+  r.start = cta * p.stream_len;
   r.end = min(r.start + p.stream_len, total);
-  r.n_seg = r.start < r.end
-                ? static_cast<int>((r.end - 1) / nbp - r.start / nbp + 1)
-                : 0;
+  r.n_seg = r.start < r.end ? (r.end - 1) / nbp - r.start / nbp + 1 : 0;
   return r;
 }
 
@@ -96,19 +97,22 @@ __device__ __forceinline__ StreamSeg stream_segment(const FwdParams& p,
                                                     const StreamRange& r,
                                                     int n_pairs, int nbp,
                                                     int si) {
-  const int64_t g = (r.end - 1) / nbp - si;
-  const int64_t s = max(r.start, g * nbp) - g * nbp;
-  const int64_t e = min(r.end, (g + 1) * nbp) - g * nbp;
+  const unsigned unbp = static_cast<unsigned>(nbp);
+  const int g = static_cast<int>(static_cast<unsigned>(r.end - 1) / unbp) -
+                si;
+  const int s = max(r.start, g * nbp) - g * nbp;
+  const int e = min(r.end, (g + 1) * nbp) - g * nbp;
   StreamSeg sg;
-  sg.j0 = static_cast<int>(s);
-  sg.n = static_cast<int>(e - s);
-  sg.first = static_cast<int>(s);
+  sg.j0 = s;
+  sg.n = e - s;
+  sg.first = s;
   sg.kind = e < nbp ? kSegWriter : (s > 0 ? kSegMerger : kSegWhole);
-  sg.first_cta = static_cast<int>((g * nbp) / p.stream_len);
-  sg.pair = static_cast<int>(g % n_pairs);
-  const int64_t bh = g / n_pairs;
-  sg.hq = static_cast<int>(bh % p.Hq);
-  sg.b = static_cast<int>(bh / p.Hq);
+  sg.first_cta = static_cast<int>(static_cast<unsigned>(g * nbp) /
+                                  static_cast<unsigned>(p.stream_len));
+  const unsigned bh = static_cast<unsigned>(g) / static_cast<unsigned>(n_pairs);
+  sg.pair = g - static_cast<int>(bh) * n_pairs;
+  sg.b = static_cast<int>(bh / static_cast<unsigned>(p.Hq));
+  sg.hq = static_cast<int>(bh) - sg.b * p.Hq;
   return sg;
 }
 

@@ -34,6 +34,9 @@ def sched(B, Hq, Hkv, Nq, Nkv, D, causal=False, sms=152):
     ((1, 5, 5, 4096, 4096, 128), "stream"),    # 80 pairs, 4096 keys
     ((1, 5, 5, 4096, 2048, 128), "plain"),     # short rows: overhead wins
     ((1, 5, 5, 4096, 8192, 64), "stream"),
+    ((1, 8, 8, 4096, 8192, 64), "stream"),     # 128 pairs at D = 64
+    ((1, 16, 16, 4096, 4096, 64), "stream"),   # 256 pairs, 4096 keys
+    ((1, 9, 9, 4096, 8192, 64), "plain"),      # 144 pairs
     # few pairs: split-KV while its pieces fit one wave, else stream
     ((1, 4, 4, 2048, 16384, 128), "split_kv"),   # 16 pairs x 4 pieces
     ((4, 8, 8, 512, 8192, 128), "split_kv"),     # 64 pairs x 2 pieces
@@ -48,7 +51,9 @@ def test_choices_measured_on_gb300(shape, kind):
     vs 113 at 144, 33 vs 38 on 2048-key rows; split against stream: 66 vs
     72 us for 16 pairs of 16384 keys, 68 vs 71 for 64 pairs of 8192; stream
     against a split of more than one wave: 112 vs 136 us for 64 pairs of
-    16384 keys, 89 vs 101 at D = 64, 194 vs 209 for 32 pairs of 32768)."""
+    16384 keys, 89 vs 101 at D = 64, 194 vs 209 for 32 pairs of 32768; at
+    D = 64 stream 83 vs 90 us at 128 pairs and 87 vs 94 at 256 pairs of
+    4096 keys, plain 90 vs 93 at 144 pairs)."""
     assert sched(*shape)["kind"] == kind
 
 
