@@ -363,6 +363,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(sQ + x * C::kQKTileBytes + c * kBoxBytes, &tmQ,
                         bQFull, c * C::kQKBoxCols, row0 + x * kBM, zq, once);
         q_loads = si + 1;
+        // The next segment's Q goes to L2 now: it loads into the one Q
+        // buffer only once this segment's last S is issued, and the next
+        // segment's first S waits for it.
+        if (si + 1 < n_seg()) {
+          const StreamSeg sn = stream_segment(p, range(), n_pairs, nbp, si + 1);
+          const int row0n = sn.pair * (2 * kBM);
+          const int zqn = sn.b * p.Hq + sn.hq;
+          for (int x = 0; x < (row0n + kBM < p.Nq ? 2 : 1); ++x)
+            for (int c = 0; c < C::kQKBoxes; ++c)
+              tma_prefetch_l2_3d(&tmQ, c * C::kQKBoxCols, row0n + x * kBM, zqn);
+        }
         int j = sg.first;                        // block index in the pair
         for (int i = 0; i < sg.n; ++i, ++r, j = (j + 1 == sg.j0 + sg.n)
                                                     ? sg.j0 : j + 1) {
