@@ -14,6 +14,7 @@ same for pinned host tensors: it copies the inputs to the device, runs the
 kernel and copies O and LSE back, all on the current stream.
 """
 
+import contextlib
 import ctypes
 import math
 import os
@@ -474,15 +475,18 @@ def fwd_host(q, k, v, scale=None, causal=False, device="cuda", bufs=None):
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     # the library works on the current device: make it the buffers' one
-    with torch.cuda.device(dev):
+    # (entering the device context only when it differs: the call is
+    # timed end to end, and the context costs microseconds)
+    ctx = (contextlib.nullcontext() if torch.cuda.current_device() == dev.index
+           else torch.cuda.device(dev))
+    with ctx:
         stream = torch.cuda.current_stream(dev)
-        p = [t.data_ptr() for t in (q, k, v, bufs["o_h"], bufs["lse_h"],
-                                    bufs["q"], bufs["k"], bufs["v"],
-                                    bufs["o"], bufs["lse"])]
-        st = int(load().fa_fwd_host(*[ctypes.c_void_p(x) for x in p], B, Hq,
-                                    Hkv, Nq, Nkv, D, ctypes.c_float(scale),
-                                    1 if causal else 0,
-                                    ctypes.c_void_p(stream.cuda_stream)))
+        st = int(load().fa_fwd_host(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), bufs["o_h"].data_ptr(),
+            bufs["lse_h"].data_ptr(), bufs["q"].data_ptr(),
+            bufs["k"].data_ptr(), bufs["v"].data_ptr(), bufs["o"].data_ptr(),
+            bufs["lse"].data_ptr(), B, Hq, Hkv, Nq, Nkv, D, scale,
+            1 if causal else 0, stream.cuda_stream))
         if st != FA_OK:
             raise FAError(st, "fa_fwd_host")
         stream.synchronize()
