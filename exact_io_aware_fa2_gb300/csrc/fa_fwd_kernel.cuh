@@ -63,6 +63,9 @@ constexpr int kMmaWarp = 0;
 constexpr int kLoadWarp = 1;
 constexpr int kSoftmaxWarp0 = 2;
 constexpr float kRescaleLog2 = 8.0f;
+// K/V bytes of the query-head groups the one-pair-per-CTA causal grid runs
+// together (see fa_fwd_kernel): two heads of 32768 keys at head dim 128.
+constexpr int64_t kCausalGroupKVBytes = 40ll << 20;
 constexpr uint32_t kTmemCols = 512;
 
 // QK8: Q and K are e4m3 (one byte per element) and S = Q K^T runs as
@@ -518,13 +521,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- work item: (batch b, query head hq, tile pair) ----
   const int n_pairs = gridDim.x;
-  const int pair = CAUSAL ? (n_pairs - 1 - static_cast<int>(blockIdx.x))
-                          : static_cast<int>(blockIdx.x);
-  const int hq = blockIdx.y;
+  int pair = CAUSAL ? (n_pairs - 1 - static_cast<int>(blockIdx.x))
+                    : static_cast<int>(blockIdx.x);
+  int hq = blockIdx.y;
   const int splits = SPLIT ? p.kv_splits : 1;
-  const int b = SPLIT ? static_cast<int>(blockIdx.z) / splits
-                      : static_cast<int>(blockIdx.z);
+  int b = SPLIT ? static_cast<int>(blockIdx.z) / splits
+                : static_cast<int>(blockIdx.z);
   const int split = SPLIT ? static_cast<int>(blockIdx.z) - b * splits : 0;
+  if constexpr (CAUSAL && !SPLIT) {
+    // CTAs start in grid order (x fastest).  With a causal mask the pairs
+    // differ in length, and one head's pairs longest first, head after
+    // head, leave the SMs unevenly loaded at every head's end; all pairs of
+    // the call longest first keep every head's K/V in use at once.  So the
+    // heads go in groups whose K/V together stay within kCausalGroupKVBytes
+    // (and so in L2), and each group's pairs longest first, its heads
+    // interleaved: a static list the hardware's in-order start deals out.
+    const int G = p.Hq / p.Hkv;
+    const int64_t kv_head = 4ll * p.Nkv * D;              // K and V, bf16
+    const int gkv = static_cast<int>(
+        max(int64_t{1}, kCausalGroupKVBytes / max(kv_head, int64_t{1})));
+    const int BH = static_cast<int>(gridDim.y * gridDim.z);
+    const int gsz = min(BH, gkv * G);
+    const int i = static_cast<int>(blockIdx.x) +
+                  n_pairs * (static_cast<int>(blockIdx.y) +
+                             static_cast<int>(gridDim.y) *
+                                 static_cast<int>(blockIdx.z));
+    const int span = gsz * n_pairs;                  // items of a full group
+    const int g = i / span;
+    const int k = i - g * span;
+    const int ng = min(gsz, BH - g * gsz);           // heads in this group
+    pair = n_pairs - 1 - k / ng;
+    const int bh = g * gsz + k % ng;
+    b = bh / p.Hq;
+    hq = bh - b * p.Hq;
+  }
   const int hk = hq / (p.Hq / p.Hkv);
   const int row0[2] = {pair * (2 * kBM), pair * (2 * kBM) + kBM};
   const bool has_b = row0[1] < p.Nq;
