@@ -63,8 +63,8 @@ constexpr int kMmaWarp = 0;
 constexpr int kLoadWarp = 1;
 constexpr int kSoftmaxWarp0 = 2;
 constexpr float kRescaleLog2 = 8.0f;
-// K/V bytes of the query-head groups the one-pair-per-CTA causal grid runs
-// together (see fa_fwd_kernel): two heads of 32768 keys at head dim 128.
+// K/V bytes of the head groups a causal grid of one-unit CTAs runs
+// together (see causal_grid_item): two heads of 32768 keys at head dim 128.
 constexpr int64_t kCausalGroupKVBytes = 40ll << 20;
 constexpr uint32_t kTmemCols = 512;
 
@@ -194,6 +194,38 @@ template <bool CAUSAL>
 __device__ __forceinline__ int kv_blocks(int row0, int Nkv) {
   const int end = CAUSAL ? min(Nkv, row0 + kBM) : Nkv;
   return (end + kBN - 1) / kBN;
+}
+
+// The work unit (unit, head hq, batch b) of this CTA for a causal grid of
+// (units, Hq, B) CTAs that start in grid order (x fastest).  With a causal
+// mask the units (query-row ranges) differ in length, and one head's units
+// longest first, head after head, leave the SMs unevenly loaded at every
+// head's end; all units of the call longest first keep every head's K/V in
+// use at once.  So the heads go in groups whose K and V (kv_head_bytes per
+// KV head) together stay within kCausalGroupKVBytes, and so in L2, and each
+// group's units longest first with its heads interleaved: a static list
+// the hardware's in-order start deals out.
+__device__ __forceinline__ void causal_grid_item(const FwdParams& p,
+                                                 int64_t kv_head_bytes,
+                                                 int& unit, int& hq, int& b) {
+  const int n_units = static_cast<int>(gridDim.x);
+  const int G = p.Hq / p.Hkv;
+  const int gkv = static_cast<int>(max(
+      int64_t{1}, kCausalGroupKVBytes / max(kv_head_bytes, int64_t{1})));
+  const int BH = static_cast<int>(gridDim.y * gridDim.z);
+  const int gsz = min(BH, gkv * G);
+  const int i = static_cast<int>(blockIdx.x) +
+                n_units * (static_cast<int>(blockIdx.y) +
+                           static_cast<int>(gridDim.y) *
+                               static_cast<int>(blockIdx.z));
+  const int span = gsz * n_units;                  // items of a full group
+  const int g = i / span;
+  const int k = i - g * span;
+  const int ng = min(gsz, BH - g * gsz);           // heads in this group
+  unit = n_units - 1 - k / ng;
+  const int bh = g * gsz + k % ng;
+  b = bh / p.Hq;
+  hq = bh - b * p.Hq;
 }
 
 // P = exp2(s * c - m) for the N scores of one row (sr, fp32 bit patterns),
@@ -528,33 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int b = SPLIT ? static_cast<int>(blockIdx.z) / splits
                 : static_cast<int>(blockIdx.z);
   const int split = SPLIT ? static_cast<int>(blockIdx.z) - b * splits : 0;
-  if constexpr (CAUSAL && !SPLIT) {
-    // CTAs start in grid order (x fastest).  With a causal mask the pairs
-    // differ in length, and one head's pairs longest first, head after
-    // head, leave the SMs unevenly loaded at every head's end; all pairs of
-    // the call longest first keep every head's K/V in use at once.  So the
-    // heads go in groups whose K/V together stay within kCausalGroupKVBytes
-    // (and so in L2), and each group's pairs longest first, its heads
-    // interleaved: a static list the hardware's in-order start deals out.
-    const int G = p.Hq / p.Hkv;
-    const int64_t kv_head = 4ll * p.Nkv * D;              // K and V, bf16
-    const int gkv = static_cast<int>(
-        max(int64_t{1}, kCausalGroupKVBytes / max(kv_head, int64_t{1})));
-    const int BH = static_cast<int>(gridDim.y * gridDim.z);
-    const int gsz = min(BH, gkv * G);
-    const int i = static_cast<int>(blockIdx.x) +
-                  n_pairs * (static_cast<int>(blockIdx.y) +
-                             static_cast<int>(gridDim.y) *
-                                 static_cast<int>(blockIdx.z));
-    const int span = gsz * n_pairs;                  // items of a full group
-    const int g = i / span;
-    const int k = i - g * span;
-    const int ng = min(gsz, BH - g * gsz);           // heads in this group
-    pair = n_pairs - 1 - k / ng;
-    const int bh = g * gsz + k % ng;
-    b = bh / p.Hq;
-    hq = bh - b * p.Hq;
-  }
+  if constexpr (CAUSAL && !SPLIT)
+    causal_grid_item(p, 4ll * p.Nkv * D, pair, hq, b);   // see there
   const int hk = hq / (p.Hq / p.Hkv);
   const int row0[2] = {pair * (2 * kBM), pair * (2 * kBM) + kBM};
   const bool has_b = row0[1] < p.Nq;

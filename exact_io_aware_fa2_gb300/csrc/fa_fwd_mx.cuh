@@ -155,10 +155,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const int lane = threadIdx.x & 31;
 
   // ---- work item: (batch b, query head hq, 128-row tile) ----
-  const int tile = CAUSAL ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
-                          : static_cast<int>(blockIdx.x);
-  const int hq = blockIdx.y;
-  const int b = blockIdx.z;
+  int tile = CAUSAL ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
+                    : static_cast<int>(blockIdx.x);
+  int hq = blockIdx.y;
+  int b = blockIdx.z;
+  // K (e4m3) and V (bf16) of a KV head
+  if constexpr (CAUSAL) causal_grid_item(p, 3ll * p.Nkv * 128, tile, hq, b);
   const int hk = hq / (p.Hq / p.Hkv);
   const int row0 = tile * kBM;
   const int kv_end = CAUSAL ? min(p.Nkv, row0 + kBM) : p.Nkv;

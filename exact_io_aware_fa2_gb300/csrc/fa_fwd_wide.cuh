@@ -139,13 +139,15 @@ __global__ void __launch_bounds__(kWideThreads, WideCfg<D>::kCtasPerSm)
   const int lane = threadIdx.x & 31;
 
   // ---- work item: (batch b, query head hq, 128-row tile) ----
-  const int tile = CAUSAL ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
-                          : static_cast<int>(blockIdx.x);
-  const int hq = blockIdx.y;
+  int tile = CAUSAL ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
+                    : static_cast<int>(blockIdx.x);
+  int hq = blockIdx.y;
   const int splits = SPLIT ? p.kv_splits : 1;
-  const int b = SPLIT ? static_cast<int>(blockIdx.z) / splits
-                      : static_cast<int>(blockIdx.z);
+  int b = SPLIT ? static_cast<int>(blockIdx.z) / splits
+                : static_cast<int>(blockIdx.z);
   const int split = SPLIT ? static_cast<int>(blockIdx.z) - b * splits : 0;
+  if constexpr (CAUSAL && !SPLIT)
+    causal_grid_item(p, 4ll * p.Nkv * D, tile, hq, b);   // head groups
   const int hk = hq / (p.Hq / p.Hkv);
   const int row0 = tile * kBM;
   const int kv_end = CAUSAL ? min(p.Nkv, row0 + kBM) : p.Nkv;
