@@ -544,3 +544,31 @@ def test_zero_scale_on_a_persistent_shape():
     O, L = oracle.attention_fp64(q[1:2, 3:4].cpu(), k[1:2, 1:2].cpu(),
                                  v[1:2, 1:2].cpu(), 0.0, True)
     print(check(o1[1:2, 3:4].cpu(), l1[1:2, 3:4].cpu(), O, L, "scale 0"))
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,D", [
+    (1, 11, 11, 20000, 128),    # two-tile kernel: head groups 3, 3, 3, 2
+    (1, 7, 7, 12000, 256),      # one-tile kernel: head groups 3, 3, 1
+    (3, 4, 2, 12000, 192),      # one-tile kernel, GQA: a group spans batches
+])
+def test_causal_grid_order_covers_every_tile(B, Hq, Hkv, N, D):
+    """Causal grids of one-unit CTAs run their units by head groups, longest
+    first with the group's heads interleaved (a permutation of the grid):
+    every row of every head is written exactly once (O starts as NaN), and
+    sampled rows of the first, a middle and the last head match the
+    oracle."""
+    q, k, v = make_custom(B, Hq, Hkv, N, N, D, seed=N + D)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    assert fa.schedule(B, Hq, Hkv, N, N, D, True)["kind"] == "plain"
+    o = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, Hq, N), float("nan"), device="cuda")
+    scale = 1.0 / math.sqrt(D)
+    fa.fwd(qd, kd, vd, scale=scale, causal=True, out=o, lse=lse, check=True)
+    o, lse = o.cpu(), lse.cpu()
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    gen = torch.Generator().manual_seed(1)
+    for b, h in {(0, 0), (B - 1, Hq // 2), (B - 1, Hq - 1)}:
+        rows = _sample_rows(N, gen)
+        O, L = oracle.attention_rows_fp64(q, k, v, scale, True, b, h, rows)
+        print(check(o[b, h, rows], lse[b, h, rows], O, L,
+                    f"grid order B{B} H{Hq}/{Hkv} N{N} D{D} b{b} h{h}"))
