@@ -275,27 +275,27 @@ int plan_splits(int B, int Hq, int Nq, int Nkv, int D, int causal, int sms) {
 // Stream schedule (fa_fwd_stream.cuh; two-tile kernel, no causal mask):
 // when whole tile pairs leave SMs idle in their last wave, give every CTA
 // an equal contiguous share of all (pair, K/V block) items instead.  Costs
-// in units of one K/V block of one pair on the two-tile kernel, fitted to
-// GB300 timings of both schedules:
-//   plain  = waves x blocks per pair + pair_overhead
+// in units of one K/V block of one pair on the two-tile kernel, fitted by
+// least squares to GB300 timings of both schedules on 21 shapes per head
+// dim (80 to 256 pairs of 4096 to 32768 keys):
+//   plain  = waves x (blocks per pair + wave_overhead) + plain_overhead
 //   stream = block_factor x blocks per CTA + stream_overhead
 //            + segment_cost x (segments per CTA - 1)
-// At D = 128 (80 to 256 pairs; 2048, 4096 and 8192 keys) the stream
-// kernel's blocks are 9% slower and its partial writes, merges and segment
-// switches cost about 9 blocks more than the plain kernel's start-up and
-// epilogue; at D = 64 (22 shapes of 32 to 256 pairs and 4096 to 32768
-// keys, least squares) its blocks are as fast and the rest costs about 9
-// blocks more.  Stream runs when estimated at least kStreamGain faster and
-// a CTA's share is at least half a pair (a merger then combines at most
-// two partials).  Measured, stream against plain at D = 128: 80 pairs 71.7
-// vs 98.3 us, 112 pairs 89.2 vs 98.5, 200 pairs 148.8 vs 192.5, 128 pairs
-// 100.5 vs 100.4 (plain kept); at D = 64 and 128 pairs 83.2 vs 90.1.
+// The stream kernel's blocks take about as long as the plain kernel's; its
+// partial writes, merges and segment switches cost about 6 blocks more
+// than the plain kernel's start-up and epilogue.  Stream runs when its
+// estimate is the smaller one and a CTA's share is at least half a pair (a
+// merger then combines at most two partials); on the 42 shapes the choice
+// is within 0.6% of the faster schedule.  Measured, stream against plain
+// at D = 128: 80 pairs 70.6 vs 98.3 us, 112 pairs 87.0 vs 98.3, 128 pairs
+// 96.3 vs 98.3, 144 pairs 106.5 vs 100.4 (plain), 256 pairs 177.1 vs 192.5;
+// at D = 64 and 128 pairs 84.1 vs 90.1.
 struct StreamCost {
-  double pair_overhead, block_factor, stream_overhead, segment_cost;
+  double wave_overhead, plain_overhead, block_factor, stream_overhead,
+      segment_cost;
 };
-constexpr StreamCost kStreamCostD128{6.2, 1.09, 13.2, 2.5};
-constexpr StreamCost kStreamCostD64{8.8, 0.98, 17.4, 0.0};
-constexpr double kStreamGain = 0.98;
+constexpr StreamCost kStreamCostD128{4.06, 4.52, 1.024, 14.39, 2.08};
+constexpr StreamCost kStreamCostD64{1.46, 6.50, 0.988, 12.35, 1.48};
 
 // Schedule forced by fa_set_schedule (FA_SCHEDULE_AUTO: the estimate).
 std::atomic<int> g_forced_schedule{FA_SCHEDULE_AUTO};
@@ -365,12 +365,15 @@ Plan plan_forward(int B, int Hq, int Hkv, int Nq, int Nkv, int D,
   if (forced != FA_SCHEDULE_STREAM && !from_split) {
     const StreamCost& k = D == 64 ? kStreamCostD64 : kStreamCostD128;
     const int64_t waves = (pairs + sms - 1) / sms;
-    const double plain = static_cast<double>(waves * nbp) + k.pair_overhead;
+    const double plain =
+        static_cast<double>(waves) * (static_cast<double>(nbp) +
+                                      k.wave_overhead) +
+        k.plain_overhead;
     const int64_t segments = (L - 1 + nbp - 1) / nbp + 1;   // at most
     const double stream = k.block_factor * static_cast<double>(L) +
                           k.stream_overhead +
                           k.segment_cost * static_cast<double>(segments - 1);
-    if (2 * L < nbp || stream > kStreamGain * plain) return pl;
+    if (2 * L < nbp || stream > plain) return pl;
   }
   pl.stream_len = static_cast<int>(L);
   pl.stream_ctas = static_cast<int>((total + L - 1) / L);
@@ -557,14 +560,21 @@ int launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             ((p.Nkv + fa::kBN - 1) / fa::kBN);
       const dim3 sgrid(static_cast<unsigned>(
           (total + p.stream_len - 1) / p.stream_len));
-      // the CTAs' ticket counter starts at zero on every launch
-      if (cudaMemsetAsync(reinterpret_cast<char*>(p.work) +
-                              fa::stream_ticket_offset<D>(sgrid.x),
-                          0, 8, stream) != cudaSuccess)
+      // cooperative: every CTA resident at once, since mergers wait for
+      // writers of lower grid index (at most one CTA per SM)
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = sgrid;
+      cfg.blockDim = dim3(fa::kThreads);
+      cfg.dynamicSmemBytes = fa::StreamCfg<D, QK8>::kSmemBytes;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeCooperative;
+      attr[0].val.cooperative = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&cfg, fa::fa_fwd_stream_kernel<D, QK8>, q, k, v,
+                             o, p) != cudaSuccess)
         return FA_ERR_CUDA;
-      fa::fa_fwd_stream_kernel<D, QK8>
-          <<<sgrid, fa::kThreads, fa::StreamCfg<D, QK8>::kSmemBytes,
-             stream>>>(q, k, v, o, p);
       return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
     }
   }

@@ -26,13 +26,12 @@
 //
 // Ordering: a CTA runs its segments from its last pair down to its first,
 // so its writer segment (if any) comes first and its merger segment (if
-// any) last, and a merger depends only on CTAs with lower indices, whose
-// writer segments ran at their start.  The index is not the CTA's grid
-// index but a ticket each CTA draws from a counter in the scratch (zeroed
-// before the launch) when it starts: a lower index then always belongs to a
-// CTA that is already running, whatever order the hardware starts CTAs in
-// and whatever else shares the GPU.  Every wait is bounded and reports
-// FA_ERR_TIMEOUT if it runs out.  A writer publishes its
+// any) last, and a merger depends only on CTAs with lower grid indices,
+// whose writer segments ran at their start.  The grid is launched
+// cooperatively (at most one CTA per SM), so every CTA is resident from the
+// start and every writer a merger waits for is running, whatever order the
+// hardware starts CTAs in and whatever else shares the GPU.  Every wait is
+// bounded and reports FA_ERR_TIMEOUT if it runs out.  A writer publishes its
 // partial per softmax warp with a fence and a release store of the launch's
 // epoch to a flag, once the next segment's first scores exist (its stores
 // have drained by then); the merger's warp waits (bounded, acquire) for that
@@ -119,20 +118,15 @@ __device__ __forceinline__ StreamSeg stream_segment(const FwdParams& p,
 // Scratch of a stream launch of G CTAs: G partial slots of
 // stream_slot_floats() floats each (O as [D/4][256] float4, then m[256],
 // l[256] (exact row sums) and w[256] (row sums of the bf16 weights)), then
-// G * 8 64-bit flags (one per softmax warp of each CTA), then the 64-bit
-// ticket counter (zeroed before each launch) and 8 bytes of padding.
+// G * 8 64-bit flags (one per softmax warp of each CTA).
 template <int D>
 __host__ __device__ constexpr int64_t stream_slot_floats() {
   return static_cast<int64_t>(kTilesPerCta * kBM) * (D + 3);
 }
 constexpr int kStreamFlagsPerCta = 8;
 template <int D>
-__host__ __device__ constexpr int64_t stream_ticket_offset(int64_t ctas) {
-  return ctas * stream_slot_floats<D>() * 4 + ctas * kStreamFlagsPerCta * 8;
-}
-template <int D>
 __host__ __device__ constexpr int64_t stream_workspace_bytes(int64_t ctas) {
-  return stream_ticket_offset<D>(ctas) + 16;
+  return ctas * stream_slot_floats<D>() * 4 + ctas * kStreamFlagsPerCta * 8;
 }
 
 __device__ __forceinline__ void prefetch_l1(const void* ptr) {
@@ -254,19 +248,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_pairs = (p.Nq + 2 * kBM - 1) / (2 * kBM);
   const int nbp = (p.Nkv + kBN - 1) / kBN;          // K/V blocks per pair
 
-  // This CTA's index: a ticket drawn when it starts (see the header).  The
-  // index and the CTA's range of items sit in shared memory and are read
+  // This CTA's index and range of items sit in shared memory and are read
   // where used, which keeps them out of the registers of the block loops.
   __shared__ StreamRange range_s;
   __shared__ int cta_s;
   if (threadIdx.x == 0) {
-    const int t = static_cast<int>(atomicAdd(
-        reinterpret_cast<unsigned long long*>(
-            reinterpret_cast<char*>(p.work) +
-            stream_ticket_offset<D>(gridDim.x)),
-        1ull));
-    cta_s = t;
-    range_s = stream_range(p, n_pairs, nbp, t);
+    cta_s = static_cast<int>(blockIdx.x);
+    range_s = stream_range(p, n_pairs, nbp, static_cast<int>(blockIdx.x));
   }
   __syncthreads();
   auto cta_index = [&]() -> int { return *static_cast<volatile int*>(&cta_s); };

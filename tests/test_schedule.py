@@ -26,8 +26,10 @@ def sched(B, Hq, Hkv, Nq, Nkv, D, causal=False, sms=152):
 
 
 @pytest.mark.parametrize("shape,kind", [
-    ((1, 8, 8, 4096, 8192, 128), "plain"),     # 128 pairs: 84% of a wave
+    ((1, 8, 8, 4096, 8192, 128), "stream"),    # 128 pairs: 84% of a wave
     ((1, 9, 9, 4096, 8192, 128), "plain"),     # 144 pairs
+    ((1, 16, 16, 4096, 8192, 128), "stream"),  # 256 pairs: 1.7 waves
+    ((1, 8, 8, 4096, 4096, 128), "plain"),     # 128 pairs, 4096 keys
     ((1, 5, 5, 4096, 8192, 128), "stream"),    # 80 pairs: 53% of a wave
     ((1, 7, 7, 4096, 8192, 128), "stream"),    # 112 pairs
     ((1, 25, 25, 2048, 8192, 128), "stream"),  # 200 pairs: 1.3 waves
@@ -46,21 +48,24 @@ def sched(B, Hq, Hkv, Nq, Nkv, D, causal=False, sms=152):
 ])
 def test_choices_measured_on_gb300(shape, kind):
     """The estimate picks the schedule measured faster on GB300 (stream
-    against plain: 74 vs 99 us at 80 pairs, 95 vs 99 at 112, 156 vs 189 at
-    200 pairs, 50 vs 55 with 4096 keys; plain: 99 vs 105 at 128 pairs, 101
-    vs 113 at 144, 33 vs 38 on 2048-key rows; split against stream: 66 vs
+    against plain: 71 vs 98 us at 80 pairs, 87 vs 98 at 112, 96 vs 98 at
+    128, 177 vs 193 at 256, 144 vs 191 at 200 pairs of 2048 rows, 47 vs 55
+    with 4096 keys; plain: 100 vs 107 at 144 pairs, 55 vs 59 at 128 pairs
+    of 4096 keys, 33 vs 38 on 2048-key rows; split against stream: 66 vs
     72 us for 16 pairs of 16384 keys, 68 vs 71 for 64 pairs of 8192; stream
     against a split of more than one wave: 112 vs 136 us for 64 pairs of
     16384 keys, 89 vs 101 at D = 64, 194 vs 209 for 32 pairs of 32768; at
-    D = 64 stream 83 vs 90 us at 128 pairs and 87 vs 94 at 256 pairs of
-    4096 keys, plain 90 vs 93 at 144 pairs)."""
+    D = 64 stream 84 vs 90 us at 128 pairs and 86 vs 93 at 256 pairs of
+    4096 keys, plain 90 vs 92 at 144 pairs)."""
     assert sched(*shape)["kind"] == kind
 
 
-def test_headline_runs_one_pair_per_cta():
+def test_headline_runs_the_stream_schedule():
+    # 128 pairs x 64 blocks over 152 CTAs: 54 blocks each, one partial slot
+    # and eight flags per CTA
     s = sched(1, 8, 8, 4096, 8192, 128)
-    assert s == {"kind": "plain", "ctas": 128, "pieces": 1,
-                 "blocks_per_cta": 0, "workspace": 0}
+    assert s == {"kind": "stream", "ctas": 152, "pieces": 1,
+                 "blocks_per_cta": 54, "workspace": 152 * (SLOT[128] + 64)}
 
 
 def test_decode_shape_splits_packed_gqa():
@@ -116,7 +121,7 @@ def test_forced_settings():
     # one block per CTA when there are fewer blocks than SMs: 2 pairs of 24
     s = sched(1, 2, 2, 256, 3000, 128)
     assert s["kind"] == "stream" and s["blocks_per_cta"] == 1
-    assert s["ctas"] == 48 and s["workspace"] == 48 * (SLOT[128] + 64) + 16
+    assert s["ctas"] == 48 and s["workspace"] == 48 * (SLOT[128] + 64)
     fa.set_schedule("auto")
     assert sched(1, 2, 2, 256, 3000, 128)["kind"] != "stream"
 
@@ -180,4 +185,4 @@ def test_invariants(sms):
                 # at least half a pair per CTA, unless the shape would
                 # otherwise split into more than one wave
                 assert 2 * L >= nbp or units * 2 <= sms, what
-                assert s["workspace"] == s["ctas"] * (SLOT[D] + 64) + 16, what
+                assert s["workspace"] == s["ctas"] * (SLOT[D] + 64), what

@@ -135,11 +135,11 @@ def test_stream_repeatable_and_noalloc_identical(forced_stream):
 
 def test_stream_workspace_size(forced_stream):
     """One fp32 slot of 256 x (D + 3) words (O, m, and two row sums) and
-    eight 8-byte flags per CTA, then a 16-byte ticket counter."""
+    eight 8-byte flags per CTA."""
     _needs_gb300_sm_count()
     for B, Hq, Hkv, Nq, Nkv, D, _ in CASES:
         sch = fa.schedule(B, Hq, Hkv, Nq, Nkv, D, False)
-        want = sch["ctas"] * (256 * (D + 3) * 4 + 8 * 8) + 16
+        want = sch["ctas"] * (256 * (D + 3) * 4 + 8 * 8)
         assert fa.workspace_size(B, Hq, Hkv, Nq, Nkv, D, False) == want
 
 
