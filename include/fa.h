@@ -224,9 +224,13 @@ enum {
  *                    their last wave.  A pair cut between CTAs is finished
  *                    by the CTA holding its last block, which combines the
  *                    others' fp32 partials in its epilogue (no second
- *                    kernel).  It relies on CTAs being started in index
- *                    order; a wait that runs out reports FA_ERR_TIMEOUT
- *                    through fa_last_device_error.
+ *                    kernel).  The grid is a cooperative launch (all
+ *                    CTAs resident at once, at most one per SM), so every
+ *                    CTA a merger waits for is running; where the device
+ *                    cannot hold the whole grid at once (e.g. an SM limit
+ *                    set for the process) the launch fails and the call
+ *                    returns FA_ERR_CUDA.  A wait that runs out reports
+ *                    FA_ERR_TIMEOUT through fa_last_device_error.
  *                    FA_SCHEDULE_PERSIST (causal mask, D 64 or 128, bf16
  *                    Q/K, no split, K and V of the call within 96 MiB,
  *                    fewer than 2^31 pairs of query tiles):
