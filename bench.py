@@ -73,6 +73,10 @@ def parse():
                     help="steps of each SDPA backend (default: --steps)")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip timing the five specification workloads")
+    ap.add_argument("--schedule", default="auto",
+                    choices=["auto", "plain", "stream"],
+                    help="force the library's schedule (fa_set_schedule) for "
+                         "every call of the run; auto: the planner's choice")
     return ap.parse_args()
 
 
@@ -521,6 +525,7 @@ def low_precision_column(args, fa, w, q_h, k_h, v, o_bf16, lse_bf16, flush,
 
 def run_ours(args, w):
     from exact_io_aware_fa2_gb300 import fa
+    fa.set_schedule(args.schedule)
     ws, rank, local = dist_env()
     if ws > 1:
         import torch.distributed as dist
