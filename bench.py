@@ -490,8 +490,13 @@ def low_precision_column(args, fa, w, q_h, k_h, v, o_bf16, lse_bf16, flush,
     q8e, k8e = q8e.to(dev), k8e.to(dev)
     (q8m, qs), (k8m, ks) = quantize_mxfp8(q_h), quantize_mxfp8(k_h)
     q8m, k8m, qs, ks = (t.to(dev) for t in (q8m, k8m, qs, ks))
+    # the e4m3 path runs the schedule the planner gives the shape (two-tile
+    # or stream kernel in their QK8 form)
+    k_qk8 = kernel_for(w) if kernel_for(w) in ("fa_fwd_kernel",
+                                               "fa_fwd_stream_kernel") \
+        else "fa_fwd_kernel"
     runs = {
-        "qk8": ("fa_fwd_kernel (QK8)", lambda: fa.fwd_qk8(
+        "qk8": (f"{k_qk8} (QK8)", lambda: fa.fwd_qk8(
             q8e, k8e, v, scale=w.scale, q_descale=qd, k_descale=kd,
             causal=w.causal, out=o, lse=lse)),
         "mxfp8": ("fa_fwd_mx_kernel", lambda: fa.fwd_mxfp8(
