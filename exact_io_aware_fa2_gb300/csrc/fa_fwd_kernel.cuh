@@ -87,9 +87,9 @@ struct FwdCfg {
   static constexpr int kKStages = (D == 128) ? (QK8 ? 4 : 2) : 4;
   static constexpr int kVStages = (D == 128) ? 3 : 4;
   // barriers: Q of tile A, K full/empty, V full/empty, S full x2, P full
-  // x2, O final, drain, Q of tile B
+  // x2, O final, drain, Q of tile B, first half of P x2
   static constexpr int kNumBars =
-      1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1 + 1 + 1;
+      1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1 + 1 + 1 + 2;
   // + tmem slot (8 bytes with padding) + the wait state (24 bytes)
   static constexpr int kBarBytes = 8 * kNumBars + 32;
   static constexpr int kSmemBytes =
@@ -189,6 +189,24 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t a_tmem,
                  dv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc);
 }
 
+// The same P*V in two halves of the block's keys: H = 0 the first kBN/2
+// keys (4 MMAs, `acc` as in issue_pv), H = 1 the rest (always accumulating).
+template <int D, int H>
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem,
+                                              uint32_t a_tmem, uint64_t dv,
+                                              uint32_t idesc, bool acc) {
+  constexpr int k0 = H * (kBN / 32);
+  if constexpr (H == 0)
+    mma_ts_w(d_tmem, a_tmem, dv, idesc, acc ? 1u : 0u);
+  else
+    mma_ts_wc<1>(d_tmem, a_tmem + k0 * 8,
+                 dv + static_cast<uint64_t>(k0 * (2048 >> 4)), idesc);
+#pragma unroll
+  for (int kk = k0 + 1; kk < k0 + kBN / 32; ++kk)
+    mma_ts_wc<1>(d_tmem, a_tmem + kk * 8,
+                 dv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc);
+}
+
 // Number of K/V blocks a tile starting at query row `row0` visits.
 template <bool CAUSAL>
 __device__ __forceinline__ int kv_blocks(int row0, int Nkv) {
@@ -228,20 +246,19 @@ __device__ __forceinline__ void causal_grid_item(const FwdParams& p,
   hq = bh - b * p.Hq;
 }
 
-// P = exp2(s * c - m) for the N scores of one row (sr, fp32 bit patterns),
-// packed to bf16x2 into pp (N / 2 words); returns the row sum of the fp32
-// values.  With MASK, only the first n_vis keys count (the others get
-// p = 0).  The scores are scaled and shifted by one f32x2 FMA per pair;
-// exp2 runs on the MUFU.
-template <int N, bool MASK>
-__device__ __forceinline__ float exp_pack_row(const uint32_t* sr, float c,
-                                              float m_use, int n_vis,
-                                              uint32_t* pp) {
+// P = exp2(s * c - m) for the scores I0 .. I1-1 of one row (sr, fp32 bit
+// patterns), packed to bf16x2 into pp (word i / 2 for key i), their fp32
+// values added pairwise into the four f32x2 sums acc.  With MASK, only the
+// first n_vis keys count (the others get p = 0).  The scores are scaled and
+// shifted by one f32x2 FMA per pair; exp2 runs on the MUFU.
+template <int I0, int I1, bool MASK>
+__device__ __forceinline__ void exp_pack_range(const uint32_t* sr, float c,
+                                               float m_use, int n_vis,
+                                               uint32_t* pp, uint64_t* acc) {
   const uint64_t c2 = f2(c, c);
   const uint64_t nm2 = f2(-m_use, -m_use);
-  uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-  for (int i = 0; i < N; i += 2) {
+  for (int i = I0; i < I1; i += 2) {
     float x0, x1;
     f2_split(fma2(f2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])),
                   c2, nm2),
@@ -255,9 +272,23 @@ __device__ __forceinline__ float exp_pack_row(const uint32_t* sr, float c,
     acc[(i >> 1) & 3] = add2(acc[(i >> 1) & 3], f2(e0, e1));
     pp[i / 2] = pack_bf16x2(e0, e1);
   }
+}
+
+// The row sum of the four f32x2 sums of exp_pack_range.
+__device__ __forceinline__ float exp_sum(const uint64_t* acc) {
   float s0, s1;
   f2_split(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), s0, s1);
   return s0 + s1;
+}
+
+// exp_pack_range over all N keys of the row; returns the row sum.
+template <int N, bool MASK>
+__device__ __forceinline__ float exp_pack_row(const uint32_t* sr, float c,
+                                              float m_use, int n_vis,
+                                              uint32_t* pp) {
+  uint64_t acc[4] = {0, 0, 0, 0};
+  exp_pack_range<0, N, MASK>(sr, c, m_use, n_vis, pp, acc);
+  return exp_sum(acc);
 }
 
 // Rescale this row's O accumulator (TMEM at o_addr, D fp32 columns) by
@@ -278,6 +309,56 @@ __device__ __forceinline__ void rescale_o(uint32_t o_addr, float alpha) {
       orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
     tmem_st32(o_addr + cc * 32, orr);
   }
+}
+
+// rescale_o in chunks of 8 columns, for a caller that still holds the
+// block's scores in registers.
+template <int D>
+__device__ __forceinline__ void rescale_o_narrow(uint32_t o_addr,
+                                                 float alpha) {
+  if (!__any_sync(0xffffffffu, alpha != 1.f)) return;
+#pragma unroll 1
+  for (int cc = 0; cc < D / 8; ++cc) {
+    uint32_t orr[8];
+    tmem_ld8(o_addr + cc * 8, orr);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+    tmem_st8(o_addr + cc * 8, orr);
+  }
+}
+
+// exp_pack_row for one block of kBN keys, P written to TMEM in two halves:
+// the first half is stored (8 columns at a time, as computed), O rescaled by
+// alpha when the reference moved and O already holds earlier blocks
+// (`o_live`), and every lane arrives on p_half_bar (count: the tile's
+// threads) once those stores are complete, so that the first half's P*V can
+// start while the second half is computed; the second half's store is left
+// in flight.  Returns the row sum, added in the same order as exp_pack_row.
+template <int D, bool MASK>
+__device__ __forceinline__ float exp_pack_split(
+    const uint32_t* sr, float c, float m_use, int n_vis, uint32_t* pp,
+    uint32_t p_addr, uint32_t o_addr, bool o_live, float alpha,
+    uint32_t p_half_bar) {
+  uint64_t acc[4] = {0, 0, 0, 0};
+  // the first half in pieces of 16 keys (8 packed columns), each stored as
+  // soon as it is computed
+  exp_pack_range<0, 16, MASK>(sr, c, m_use, n_vis, pp, acc);
+  tmem_st8(p_addr, pp);
+  exp_pack_range<16, 32, MASK>(sr, c, m_use, n_vis, pp, acc);
+  tmem_st8(p_addr + 8, pp + 8);
+  exp_pack_range<32, 48, MASK>(sr, c, m_use, n_vis, pp, acc);
+  tmem_st8(p_addr + 16, pp + 16);
+  exp_pack_range<48, 64, MASK>(sr, c, m_use, n_vis, pp, acc);
+  tmem_st8(p_addr + 24, pp + 24);
+  if (o_live) rescale_o_narrow<D>(o_addr, alpha);
+  tmem_st_wait();
+  tc_fence_before();
+  mbar_arrive(p_half_bar);
+  exp_pack_range<kBN / 2, kBN, MASK>(sr, c, m_use, n_vis, pp, acc);
+  tmem_st32(p_addr + kBN / 4, pp + kBN / 4);
+  return exp_sum(acc);
 }
 
 // The bf16 rounding error of a block's largest weight: with s_ext the
@@ -315,12 +396,15 @@ __device__ __forceinline__ float top_rounding(float s_ext, float c,
 // one-pass form of the same recurrence with a stale reference.  INTERIOR:
 // no key of the block needs masking here (every key is visible to every row
 // of the tile, or the hidden ones already hold the extreme's identity as
-// their score, see hide_keys), and no mask code is compiled.
-template <int D, bool CAUSAL, bool INTERIOR = false>
+// their score, see hide_keys), and no mask code is compiled.  SPLIT_P: P is
+// written in two halves of the block's keys, and once the first half (and
+// any rescale of O) is stored and fenced the warp arrives on p_half_bar, so
+// that its P*V can start while the second half is computed.
+template <int D, bool CAUSAL, bool INTERIOR = false, bool SPLIT_P = false>
 __device__ __forceinline__ void softmax_block(
     uint32_t s_addr, uint32_t p_addr, uint32_t o_addr, int col0, int my_row0,
     int q_abs, int Nkv, float c, bool neg_scale, bool o_live, float& m_ref,
-    float& l_run, float& w_run) {
+    float& l_run, float& w_run, uint32_t p_half_bar = 0) {
   uint32_t sr[kBN];
   const bool need_mask =
       !INTERIOR &&
@@ -392,18 +476,28 @@ __device__ __forceinline__ void softmax_block(
 
   // ---- P = exp2(s * c - m), packed to bf16, row sums ----
   uint32_t pp[kBN / 2];
-  const float rsum = need_mask
-                         ? exp_pack_row<kBN, true>(sr, c, m_use, n_vis, pp)
-                         : exp_pack_row<kBN, false>(sr, c, m_use, kBN, pp);
+  float rsum;
+  if constexpr (SPLIT_P) {
+    rsum = need_mask
+               ? exp_pack_split<D, true>(sr, c, m_use, n_vis, pp, p_addr,
+                                         o_addr, o_live, alpha, p_half_bar)
+               : exp_pack_split<D, false>(sr, c, m_use, kBN, pp, p_addr,
+                                          o_addr, o_live, alpha, p_half_bar);
+  } else {
+    rsum = need_mask ? exp_pack_row<kBN, true>(sr, c, m_use, n_vis, pp)
+                     : exp_pack_row<kBN, false>(sr, c, m_use, kBN, pp);
+  }
 #undef S_
   l_run = l_run * alpha + rsum;
   w_run += rsum;
   m_ref = m_new;
 
-  // ---- rescale O when the reference max moved ----
-  if (o_live) rescale_o<D>(o_addr, alpha);
-  tmem_st32(p_addr, pp);
-  tmem_st32(p_addr + 32, pp + 32);
+  if constexpr (!SPLIT_P) {
+    // ---- rescale O when the reference max moved ----
+    if (o_live) rescale_o<D>(o_addr, alpha);
+    tmem_st32(p_addr, pp);
+    tmem_st32(p_addr + 32, pp + 32);
+  }
   tmem_st_wait();
   tc_fence_before();
 }
@@ -594,6 +688,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bDrain = bar(kB0 + 5);
   // Q of tile A at bQFull, of tile B here: S_A(first) waits only for Q_A
   const uint32_t bQFullB = bar(kB0 + 6);
+  // first half of tile x's P stored (see softmax_block)
+  auto bPHalf = [&](int x) { return bar(kB0 + 7 + x); };
   uint8_t* const misc = base_ptr + (sBar - base) + 8 * C::kNumBars;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   WaitState* const wstate = reinterpret_cast<WaitState*>(misc + 8);
@@ -611,6 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(bSFull(x), 1);
       mbar_init(bPFull(x), 4);
+      mbar_init(bPHalf(x), 4 * 32);
     }
     mbar_init(bOFinal, 1);
     mbar_init(bDrain, 1);
@@ -709,14 +806,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dVs = dV + static_cast<uint64_t>(sp) * kStep;
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
-        // O_x += P_x(j-1) V_{j-1}
+        // O_x += P_x(j-1) V_{j-1}, each half of the keys once its half of
+        // P is stored
         if (j >= 1 && j0 + j - 1 < nblk[x]) {
+          if (!(ok = __all_sync(kAll,
+                                mbar_wait(bPHalf(x), (j - 1) & 1, wc))))
+            break;
+          tc_fence_after();
+          issue_pv_half<D, 0>(tmem + C::col_o(x), tmem + C::col_p(x), dVs,
+                              C::kIdescPV, j > 1);
           if (!(ok = __all_sync(kAll,
                                 mbar_wait(bPFull(x), (j - 1) & 1, wc))))
             break;
           tc_fence_after();
-          issue_pv<D>(tmem + C::col_o(x), tmem + C::col_p(x), dVs,
-                      C::kIdescPV, j > 1);
+          issue_pv_half<D, 1>(tmem + C::col_o(x), tmem + C::col_p(x), dVs,
+                              C::kIdescPV, true);
         }
         // S_x(j) = Q_x K_j^T
         if (j < n_blocks && j0 + j < nblk[x]) {
@@ -758,11 +862,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mbar_wait(bSFull(x), j & 1, wc))))
         break;
       tc_fence_after();
-      softmax_block<D, CAUSAL>(tmem + lane_off + C::col_s(x),
-                               tmem + lane_off + C::col_p(x),
-                               tmem + lane_off + C::col_o(x), (j0 + j) * kBN,
-                               my_row0, q_abs, p.Nkv, c, neg_scale, j >= 1,
-                               m_ref, l_run, w_run);
+      softmax_block<D, CAUSAL, false, true>(
+          tmem + lane_off + C::col_s(x), tmem + lane_off + C::col_p(x),
+          tmem + lane_off + C::col_o(x), (j0 + j) * kBN, my_row0, q_abs,
+          p.Nkv, c, neg_scale, j >= 1, m_ref, l_run, w_run, bPHalf(x));
       __syncwarp();
       if (lane == 0) mbar_arrive(bPFull(x));
     }

@@ -87,9 +87,10 @@ struct PersistCfg {
   // current pair), one at 128 (shared memory is full).
   static constexpr int kQBufs = (D == 64) ? 2 : 1;
   // barriers: Q full/empty per buffer, K and V full/empty per stage, S full
-  // and P full per tile, O final and O empty per tile, drain
+  // and P full per tile, O final and O empty per tile, drain, first half of
+  // P per tile
   static constexpr int kNumBars =
-      2 * kQBufs + 2 * C::kKStages + 2 * C::kVStages + 2 + 2 + 2 + 2 + 1;
+      2 * kQBufs + 2 * C::kKStages + 2 * C::kVStages + 2 + 2 + 2 + 2 + 1 + 2;
   static constexpr int kBarBytes = 8 * kNumBars + 32;
   static constexpr int kSmemBytes =
       1024 + C::kQKTileBytes * (kTilesPerCta * kQBufs + C::kKStages) +
@@ -196,7 +197,12 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
   auto bOFinal = [&](int x) { return bar(kB0 + 4 + x); };
   auto bOEmpty = [&](int x) { return bar(kB0 + 6 + x); };
   const uint32_t bDrain = bar(kB0 + 8);
-  static_assert(kB0 + 9 == PC::kNumBars, "barrier count");
+  // first half of tile x's P stored (see softmax_block); P*V runs in two
+  // halves at head dim 64 (C3 53.2 -> 52.8 us), at 128 whole (the halves
+  // measured 0.8% slower on the causal GQA N 8192 shape)
+  constexpr bool kSplitP = D == 64;
+  auto bPHalf = [&](int x) { return bar(kB0 + 9 + x); };
+  static_assert(kB0 + 11 == PC::kNumBars, "barrier count");
   uint8_t* const misc = base_ptr + (sBar - base) + 8 * PC::kNumBars;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   WaitState* const wstate = reinterpret_cast<WaitState*>(misc + 8);
@@ -217,6 +223,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(bSFull(x), 1);
       mbar_init(bPFull(x), 4);
+      mbar_init(bPHalf(x), 4 * 32);
       mbar_init(bOFinal(x), 1);
       mbar_init(bOEmpty(x), 4);
     }
@@ -356,13 +363,26 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
                 !(ok = __all_sync(kAll,
                                   mbar_wait(bOEmpty(x), (r - 1) & 1, wc))))
               break;
+            if constexpr (kSplitP) {
+              // each half of the keys once its half of P is stored
+              if (!(ok = __all_sync(
+                        kAll, mbar_wait(bPHalf(x), (pph >> x) & 1u, wc))))
+                break;
+              tc_fence_after();
+              issue_pv_half<D, 0>(tmem + C::col_o(x), tmem + C::col_p(x),
+                                  dVs, C::kIdescPV, j > 1);
+            }
             if (!(ok = __all_sync(kAll, mbar_wait(bPFull(x), (pph >> x) & 1u,
                                                   wc))))
               break;
             pph ^= 1u << x;
             tc_fence_after();
-            issue_pv<D>(tmem + C::col_o(x), tmem + C::col_p(x), dVs,
-                        C::kIdescPV, j > 1);
+            if constexpr (kSplitP)
+              issue_pv_half<D, 1>(tmem + C::col_o(x), tmem + C::col_p(x),
+                                  dVs, C::kIdescPV, true);
+            else
+              issue_pv<D>(tmem + C::col_o(x), tmem + C::col_p(x), dVs,
+                          C::kIdescPV, j > 1);
             if (j == u.nblk[x]) mma_commit_w(bOFinal(x));  // O_x complete
           }
           // S_x(j) = Q_x K_j^T
@@ -471,9 +491,10 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
           hide_keys(s_at, max(0, min(kBN, lim)),
                     neg_scale ? INFINITY : -INFINITY);
         }
-        softmax_block<D, CAUSAL, true>(s_at, p_at, o_at, col0, my_row0, q_abs,
-                                       p.Nkv, c, neg_scale, j >= 1, m_ref,
-                                       l_run, w_run);
+        softmax_block<D, CAUSAL, true, kSplitP>(s_at, p_at, o_at, col0, my_row0,
+                                             q_abs, p.Nkv, c, neg_scale,
+                                             j >= 1, m_ref, l_run, w_run,
+                                             bPHalf(x));
         __syncwarp();
         if (lane == 0) mbar_arrive(bPFull(x));
       }

@@ -224,7 +224,8 @@ __device__ __forceinline__ void merge_final_row(
 template <int D, bool QK8>
 struct StreamCfg {
   using C = FwdCfg<D, QK8>;
-  // the two-tile kernel's barriers plus q_empty and o_empty
+  // the two-tile kernel's barriers (its Q of tile B unused) plus q_empty
+  // and o_empty
   static constexpr int kNumBars = C::kNumBars + 2;
   static constexpr int kSmemBytes = C::kSmemBytes + 16;
 };
@@ -286,7 +287,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bDrain = bar(kB0 + 5);
   const uint32_t bQEmpty = bar(kB0 + 6);
   const uint32_t bOEmpty = bar(kB0 + 7);
-  static_assert(kB0 + 8 <= SC::kNumBars, "barrier count");
+  // first half of tile x's P stored (see softmax_block)
+  auto bPHalf = [&](int x) { return bar(kB0 + 8 + x); };
+  static_assert(kB0 + 10 <= SC::kNumBars, "barrier count");
   uint8_t* const misc = base_ptr + (sBar - base) + 8 * SC::kNumBars;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc);
   WaitState* const wstate = reinterpret_cast<WaitState*>(misc + 8);
@@ -304,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(bSFull(x), 1);
       mbar_init(bPFull(x), 4);
+      mbar_init(bPHalf(x), 4 * 32);
     }
     mbar_init(bOFinal, 1);
     mbar_init(bDrain, 1);
@@ -436,15 +440,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           if (x == 1 && !live_b) continue;
-          // O_x += P_x(j-1) V_{j-1}
+          // O_x += P_x(j-1) V_{j-1}, each half of the keys once its half
+          // of P is stored
           if (j >= 1) {
+            if (!(ok = __all_sync(kAll, mbar_wait(bPHalf(x), (pph >> x) & 1u,
+                                                  wc))))
+              break;
+            tc_fence_after();
+            issue_pv_half<D, 0>(tmem + C::col_o(x), tmem + C::col_p(x), dVs,
+                                C::kIdescPV, j > 1);
             if (!(ok = __all_sync(kAll, mbar_wait(bPFull(x), (pph >> x) & 1u,
                                                   wc))))
               break;
             pph ^= 1u << x;
             tc_fence_after();
-            issue_pv<D>(tmem + C::col_o(x), tmem + C::col_p(x), dVs,
-                        C::kIdescPV, j > 1);
+            issue_pv_half<D, 1>(tmem + C::col_o(x), tmem + C::col_p(x), dVs,
+                                C::kIdescPV, true);
           }
           // S_x(j) = Q_x K_j^T
           if (j < n_blocks) {
@@ -530,10 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         sph ^= 1u;
         tc_fence_after();
-        softmax_block<D, false>(tmem + lane_off + C::col_s(x),
-                                tmem + lane_off + C::col_p(x), o_addr,
-                                blk * kBN, my_row0, q_abs, p.Nkv, c,
-                                neg_scale, j >= 1, m_ref, l_run, w_run);
+        softmax_block<D, false, false, true>(
+            tmem + lane_off + C::col_s(x), tmem + lane_off + C::col_p(x),
+            o_addr, blk * kBN, my_row0, q_abs, p.Nkv, c, neg_scale, j >= 1,
+            m_ref, l_run, w_run, bPHalf(x));
         __syncwarp();
         if (lane == 0) mbar_arrive(bPFull(x));
         blk = (blk + 1 == blk_end) ? blk_lo : blk + 1;
