@@ -311,8 +311,8 @@ __device__ __forceinline__ void rescale_o(uint32_t o_addr, float alpha) {
   }
 }
 
-// rescale_o in chunks of 8 columns, for a caller that still holds half of
-// the block's scores in registers.
+// rescale_o in chunks of 8 columns, for a caller that still holds the
+// block's scores in registers.
 template <int D>
 __device__ __forceinline__ void rescale_o_narrow(uint32_t o_addr,
                                                  float alpha) {
@@ -341,7 +341,6 @@ __device__ __forceinline__ float exp_pack_split(
     const uint32_t* sr, float c, float m_use, int n_vis, uint32_t* pp,
     uint32_t p_addr, uint32_t o_addr, bool o_live, float alpha,
     uint32_t p_half_bar) {
-  static_assert(kBN == 128, "the pieces below cover 128 keys");
   uint64_t acc[4] = {0, 0, 0, 0};
   // the first half in pieces of 16 keys (8 packed columns), each stored as
   // soon as it is computed
